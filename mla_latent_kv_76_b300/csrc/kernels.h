@@ -1,0 +1,54 @@
+// Host-side launch wrappers shared by the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Tokens per split-KV tile; equal to the paged block size so a tile never
+// straddles two blocks.
+constexpr int kTileTokens = 64;
+constexpr int kMaxBatch = 4096;     // decode: per-CTA prefix table lives in shared memory
+constexpr int kMaxWorkers = 4096;
+
+struct DecodeLaunch {
+  const void* q;
+  const void* pool;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  int32_t num_blocks;
+  int64_t seq_stride;
+  const int32_t* seqlens;
+  int32_t batch;
+  int32_t n_heads;
+  int32_t d_latent;
+  int32_t d_rope;
+  float scale;
+  int32_t workers;        // G
+  float* o_part;          // [(G + B)][n_h][d_c]
+  float* lse_part;        // [(G + B)][n_h]
+  void* z_out;
+  int32_t z_is_fp32;
+  float* lse_out;
+  int32_t* status;
+};
+
+// Generic (mma.sync) decode partial pass + combine.
+cudaError_t launch_decode_generic(const DecodeLaunch& a, int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const DecodeLaunch& a, cudaStream_t s);
+int generic_head_groups(int n_heads);
+size_t generic_smem_bytes(int D, int batch);
+
+cudaError_t launch_absorb(const mla_dims& d, int batch, const void* q_c, const void* q_r,
+                          const int32_t* pos, const void* w_uk, void* q_out, cudaStream_t s);
+cudaError_t launch_out_proj(const mla_dims& d, int batch, const void* z, const void* w_uv,
+                            void* o_out, cudaStream_t s);
+cudaError_t launch_append(const mla_dims& d, int n_tokens, int d_model, const void* h,
+                          const void* w, const int32_t* seq_idx, const int32_t* pos, int n_seqs,
+                          const int32_t* block_table, int max_blocks, int num_blocks,
+                          int64_t seq_stride, void* pool, int32_t* status, cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,141 @@
+"""The C ABI library: it loads, exports every symbol include/mla.h declares,
+and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mla():
+    from __graft_entry__ import build
+    build()
+    import mla_latent_kv_76_b300 as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("mla_absorb_q", "mla_append_cache", "mla_decode_attn", "mla_decode_workspace_size",
+                 "mla_out_proj", "mla_read_status", "mla_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(mla):
+    out = subprocess.run(["nm", "-D", "--defined-only", mla.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (mla_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(mla.lib, name)
+
+
+def test_build_targets_sm_103a_only():
+    from mla_latent_kv_76_b300 import build as b
+    assert b.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings_and_version(mla):
+    assert mla.mla_status_string(0) == "ok"
+    assert "workspace" in mla.mla_status_string(mla.MLA_ERR_WORKSPACE)
+    assert mla.mla_status_string(12345) == "unknown status"
+    assert mla.mla_version() >= 10000
+
+
+def _dims(mla, **kw):
+    d = dict(n_heads=128, d_head=128, d_v=128, d_latent=512, d_rope=64, block_tokens=64, rope_base=10000.0)
+    d.update(kw)
+    return mla.Dims(**d)
+
+
+def test_host_validation_rejects_bad_arguments(mla):
+    lib = mla.lib
+    d = _dims(mla)
+    # null dims / negative sizes
+    assert lib.mla_absorb_q(None, 1, 16, 16, 16, 16, 16, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_absorb_q(ctypes.byref(d), -1, 16, 16, 16, 16, 16, None) == mla.MLA_ERR_INVALID_ARG
+    # batch 0 is a no-op that succeeds without a GPU
+    assert lib.mla_absorb_q(ctypes.byref(d), 0, None, None, None, None, None, None) == mla.MLA_OK
+    assert lib.mla_out_proj(ctypes.byref(d), 0, None, None, None, None) == mla.MLA_OK
+    # null pointers
+    assert lib.mla_absorb_q(ctypes.byref(d), 2, None, 16, 16, 16, 16, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_out_proj(ctypes.byref(d), 2, 16, None, 16, None) == mla.MLA_ERR_INVALID_ARG
+    # misaligned pointer
+    assert lib.mla_out_proj(ctypes.byref(d), 2, 18, 16, 16, None) == mla.MLA_ERR_INVALID_ARG
+    # odd rope dim / bad base
+    bad = _dims(mla, d_rope=63)
+    assert lib.mla_absorb_q(ctypes.byref(bad), 1, 16, 16, 16, 16, 16, None) == mla.MLA_ERR_INVALID_ARG
+    bad = _dims(mla, rope_base=0.0)
+    assert lib.mla_out_proj(ctypes.byref(bad), 1, 16, 16, 16, None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_decode_validation(mla):
+    lib = mla.lib
+    d = _dims(mla)
+
+    def call(dd, batch=1, q=16, pool=16, bt=None, mb=0, nb=0, ss=64, sl=16, scale=0.07, nw=0, flags=0,
+             ws=16, wsb=1 << 30, z=16):
+        return lib.mla_decode_attn(ctypes.byref(dd) if dd is not None else None, batch, q, pool, bt, mb, nb, ss,
+                                   sl, scale, nw, flags, ws, wsb, z, 1, None, None, None)
+    assert call(None) == mla.MLA_ERR_INVALID_ARG
+    assert call(_dims(mla, d_latent=96)) == mla.MLA_ERR_UNSUPPORTED
+    assert call(_dims(mla, n_heads=129)) == mla.MLA_ERR_UNSUPPORTED
+    assert call(_dims(mla, d_rope=8)) == mla.MLA_ERR_UNSUPPORTED          # 520 not a multiple of 16
+    assert call(d, batch=0) == mla.MLA_OK
+    assert call(d, batch=-1) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, batch=5000) == mla.MLA_ERR_UNSUPPORTED
+    assert call(d, q=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, sl=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, scale=float("nan")) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, flags=8) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, nw=-1) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, bt=16, mb=0) == mla.MLA_ERR_INVALID_ARG                # paged without capacity
+    assert call(_dims(mla, block_tokens=32), bt=16, mb=4, nb=4) == mla.MLA_ERR_UNSUPPORTED
+    assert call(d, ss=0) == mla.MLA_ERR_INVALID_ARG                      # contiguous without stride
+    # workspace sizing: explicit worker counts need no device
+    n1 = lib.mla_decode_workspace_size(ctypes.byref(d), 16, 10)
+    n2 = lib.mla_decode_workspace_size(ctypes.byref(d), 16, 20)
+    assert n2 - n1 >= 10 * 128 * 513 * 4 and n1 >= 26 * 128 * 512 * 4
+    assert lib.mla_decode_workspace_size(ctypes.byref(_dims(mla, d_latent=96)), 16, 10) == 0
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), -1, 10) == 0
+
+
+def test_append_validation(mla):
+    lib = mla.lib
+    d = _dims(mla)
+    args = lambda **kw: dict(dict(T=1, dm=7168, h=16, w=16, si=16, pos=16, ns=1, bt=16, mb=4, nb=4, ss=0,
+                                  pool=16), **kw)
+
+    def call(dd, **kw):
+        a = args(**kw)
+        return lib.mla_append_cache(ctypes.byref(dd) if dd is not None else None, a["T"], a["dm"], a["h"],
+                                    a["w"], a["si"], a["pos"], a["ns"], a["bt"], a["mb"], a["nb"], a["ss"],
+                                    a["pool"], None, None)
+    assert call(None) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, T=0) == mla.MLA_OK
+    assert call(d, dm=7170) == mla.MLA_ERR_UNSUPPORTED
+    assert call(d, h=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, mb=0) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, bt=None, ss=0) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, ns=0) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """A copy of the package without libmla.so must refuse to import."""
+    pkg = os.path.join(ROOT, "mla_latent_kv_76_b300")
+    dst = tmp_path / "mla_latent_kv_76_b300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__"))
+    r = subprocess.run([sys.executable, "-c", "import mla_latent_kv_76_b300"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode != 0 and "libmla.so is missing" in r.stderr
