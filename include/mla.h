@@ -153,6 +153,39 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
                     void* stream);
 
 /*
+ * Decode without a caller-provided workspace.  The pages have no counterpart
+ * to this entry point; it exists for callers that cannot allocate device
+ * memory when they call decode: a plugin inside an inference server that is
+ * handed only its input and output buffers and has no allocator of its own,
+ * or a latency-critical serving loop that forbids cudaMalloc after start-up
+ * because an allocation can synchronise the device or fail under memory
+ * pressure.  It runs the same kernels as mla_decode_attn, with the split-KV
+ * partials in a file-scope device array of MLA_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * that every GPU which loads the library holds until the process exits.
+ *  - Arguments are those of mla_decode_attn without workspace/workspace_bytes.
+ *  - If mla_decode_workspace_size(dims, batch, num_workers) is larger than
+ *    MLA_NOALLOC_SCRATCH_BYTES the call returns MLA_ERR_WORKSPACE and
+ *    enqueues nothing.  (On a 148-SM B300 with 128 heads, d_c = 512 and
+ *    automatic workers this allows up to 107 sequences; passing an explicit,
+ *    smaller num_workers allows more.)
+ *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents.
+ *    Nothing in it has to start at zero: each call writes every partial it
+ *    reads back.  Calls whose GPU work overlaps (other streams, or threads
+ *    without ordering between them) race on the array and return wrong
+ *    results; serialise them, for example on one stream.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int mla_decode_attn_noalloc(const mla_dims* dims, int32_t batch, const void* q, const void* pool,
+                            const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                            int64_t seq_stride_tokens, const int32_t* seqlens, float scale,
+                            int32_t num_workers, int32_t flags, void* z_out, int32_t z_is_fp32,
+                            float* lse_out, int32_t* dev_status, void* stream);
+
+/*
  * Value up-projection after the latent sum ("为什么矩阵吸收很关键":
  * sum_j A_j W^UV c_j = W^UV sum_j A_j c_j; worked example step 5).
  *   o[b][i] = W^UV_i z[b][i]           (bf16 out, fp32 accumulate)

@@ -22,9 +22,10 @@ MLA_ERR_CUDA = 4
 MLA_ERR_DEVICE_TIMEOUT = 5
 MLA_ERR_DEVICE_BOUNDS = 6
 MLA_DECODE_FORCE_GENERIC = 1
+MLA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mla_latent_kv_76_b300.build` "
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python mla_latent_kv_76_b300/build.py` "
                       "(there is no fallback implementation)")
 
 lib = ctypes.CDLL(LIB_PATH)
@@ -59,12 +60,14 @@ lib.mla_decode_workspace_size.restype = ctypes.c_size_t
 lib.mla_decode_attn.argtypes = [_DP, _I32, _P, _P, _P, _I32, _I32, _I64, _P, ctypes.c_float, _I32, _I32,
                                 _P, ctypes.c_size_t, _P, _I32, _P, _P, _P]
 lib.mla_out_proj.argtypes = [_DP, _I32, _P, _P, _P, _P]
+lib.mla_decode_attn_noalloc.argtypes = [_DP, _I32, _P, _P, _P, _I32, _I32, _I64, _P, ctypes.c_float, _I32, _I32,
+                                        _P, _I32, _P, _P, _P]
 lib.mla_read_status.argtypes = [_P, _P, _P]
 lib.mla_status_string.argtypes = [ctypes.c_int]
 lib.mla_status_string.restype = ctypes.c_char_p
 lib.mla_version.argtypes = []
 for _fn in ("mla_absorb_q", "mla_append_cache", "mla_decode_attn", "mla_out_proj", "mla_read_status",
-            "mla_version"):
+            "mla_version", "mla_decode_attn_noalloc"):
     getattr(lib, _fn).restype = ctypes.c_int
 
 
@@ -163,6 +166,32 @@ def mla_decode_attn(dims: Dims, q, pool, seqlens, scale: float, block_table=None
         _ptr(lse_out, "lse_out", (torch.float32,)), _ptr(dev_status, "dev_status", (torch.int32,)),
         _stream(stream))
     _check("mla_decode_attn", code)
+    return z_out, lse_out
+
+
+def mla_decode_attn_noalloc(dims: Dims, q, pool, seqlens, scale: float, block_table=None, num_blocks: int = 0,
+                            seq_stride: int = 0, num_workers: int = 0, flags: int = 0, z_out=None,
+                            z_is_fp32: bool = True, lse_out=None, dev_status=None, stream=None,
+                            want_lse: bool = True):
+    """Decode with the library's built-in scratch instead of a workspace, for
+    callers that cannot allocate device memory at call time.  Outputs must be
+    passed in for the call itself to allocate nothing.  Returns (z, lse)."""
+    B = q.shape[0]
+    dev = q.device
+    if z_out is None:
+        z_out = torch.empty((B, dims.n_heads, dims.d_latent),
+                            dtype=torch.float32 if z_is_fp32 else torch.bfloat16, device=dev)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, dims.n_heads), dtype=torch.float32, device=dev)
+    max_blocks = 0 if block_table is None else block_table.shape[1]
+    code = lib.mla_decode_attn_noalloc(
+        ctypes.byref(dims), B, _ptr(q, "q", _BF16_LIKE), _ptr(pool, "pool", _BF16_LIKE),
+        _ptr(block_table, "block_table", (torch.int32,)), max_blocks, num_blocks, seq_stride,
+        _ptr(seqlens, "seqlens", (torch.int32,)), float(scale), num_workers, flags,
+        _ptr(z_out, "z_out"), 1 if z_out.dtype == torch.float32 else 0,
+        _ptr(lse_out, "lse_out", (torch.float32,)), _ptr(dev_status, "dev_status", (torch.int32,)),
+        _stream(stream))
+    _check("mla_decode_attn_noalloc", code)
     return z_out, lse_out
 
 

@@ -1,6 +1,6 @@
 """Build libmla.so in-tree with nvcc for sm_103a (B300).
 
-    python -m mla_latent_kv_76_b300.build [--force] [--verbose]
+    python mla_latent_kv_76_b300/build.py [--force] [--verbose]
 
 The library is a plain shared object (C ABI, static CUDA runtime); no torch
 extension machinery is involved.

@@ -42,8 +42,20 @@ def test_library_exports_every_declared_symbol(mla):
 
 
 def test_build_targets_sm_103a_only():
-    from mla_latent_kv_76_b300 import build as b
-    assert b.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    from __graft_entry__ import _build_module
+    assert _build_module().ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_build_works_from_a_checkout_without_the_library(tmp_path):
+    """build() must not need the library it builds (fresh clone)."""
+    dst = tmp_path / "repo"
+    shutil.copytree(ROOT, dst, ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__", ".git", "_work",
+                                                             "gpurun_out", "*.ncu-rep"))
+    r = subprocess.run([sys.executable, "-c", "import __graft_entry__ as g; g.build(); "
+                        "import mla_latent_kv_76_b300 as m; print(m.mla_version())"],
+                       cwd=dst, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().endswith("10000")
 
 
 def test_status_strings_and_version(mla):
