@@ -163,12 +163,17 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   }
   const int sms = device_sm_count();
   if (sms <= 0) return MLA_ERR_CUDA;
-  const int G = num_workers > 0 ? num_workers : auto_workers(*dims, sms);
+  DecodeLaunch a;
+  a.n_heads = dims->n_heads;
+  a.d_latent = dims->d_latent;
+  a.d_rope = dims->d_rope;
+  a.batch = batch;
+  const bool use_tc = !(flags & MLA_DECODE_FORCE_GENERIC) && mla::tc_supported(a);
+  const int G = num_workers > 0 ? num_workers : (use_tc ? (sms / 2 > 0 ? sms / 2 : 1) : auto_workers(*dims, sms));
   const WsLayout w = ws_layout(*dims, batch, G);
   if (!workspace || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
 
-  DecodeLaunch a;
   a.q = q;
   a.pool = pool;
   a.block_table = block_table;
@@ -176,10 +181,6 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.num_blocks = num_blocks;
   a.seq_stride = seq_stride_tokens;
   a.seqlens = seqlens;
-  a.batch = batch;
-  a.n_heads = dims->n_heads;
-  a.d_latent = dims->d_latent;
-  a.d_rope = dims->d_rope;
   a.scale = scale;
   a.workers = G;
   a.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_o);
@@ -189,7 +190,7 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.lse_out = lse_out;
   a.status = dev_status;
   cudaStream_t s = as_stream(stream);
-  cudaError_t e = mla::launch_decode_generic(a, sms, s);
+  cudaError_t e = use_tc ? mla::launch_decode_tc(a, s) : mla::launch_decode_generic(a, sms, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return from_cuda(mla::launch_combine(a, s));
 }

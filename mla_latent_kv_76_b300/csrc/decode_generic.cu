@@ -39,36 +39,6 @@ __host__ __device__ inline GenericSmem generic_smem(int D, int batch) {
 
 int generic_head_groups(int n_heads) { return (n_heads + kHG - 1) / kHG; }
 
-// Exclusive prefix of tiles_of(effective_len(b)) over b into pre[0..B]; block-wide.
-MLA_DEVI void tile_prefix(const DecodeLaunch& a, int64_t cap, int* pre) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  const int B = a.batch;
-  const int per = (B + nthr - 1) / nthr;
-  const int b0 = tid * per, b1 = min(B, b0 + per);
-  int local = 0;
-  for (int b = b0; b < b1; ++b) local += tiles_of(effective_len(a.seqlens, b, cap, a.status));
-  // block exclusive scan of `local` (warp shuffles + one smem pass)
-  __shared__ int warp_sums[32];
-  const int lane = tid & 31, warp = tid >> 5;
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  int warp_off = 0;
-  for (int w = 0; w < warp; ++w) warp_off += warp_sums[w];
-  int run = warp_off + incl - local;
-  for (int b = b0; b < b1; ++b) {
-    pre[b] = run;
-    run += tiles_of(effective_len(a.seqlens, b, cap, nullptr));
-  }
-  if (tid == nthr - 1) pre[B] = run;  // last thread's run is the grand total
-  __syncthreads();
-}
-
 template <int DC>
 __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -90,7 +60,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
   const float sl2 = a.scale * kLog2e;
 
-  tile_prefix(a, cap, pre);
+  tile_prefix(a.seqlens, a.batch, cap, a.status, pre);
   const int64_t T = pre[a.batch];
   const int64_t lo = worker_begin(wk, T, G), hi = worker_begin(wk + 1, T, G);
   const int chunks = D / 8;

@@ -40,6 +40,11 @@ struct DecodeLaunch {
 cudaError_t launch_decode_generic(const DecodeLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const DecodeLaunch& a, cudaStream_t s);
 int generic_head_groups(int n_heads);
+
+// Tensor-core (tcgen05) decode for n_h = 128, d_c = 512, d_R = 64: `workers`
+// is the number of CTA pairs (clusters of two).
+bool tc_supported(const DecodeLaunch& a);
+cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
 size_t generic_smem_bytes(int D, int batch);
 
 cudaError_t launch_absorb(const mla_dims& d, int batch, const void* q_c, const void* q_r,

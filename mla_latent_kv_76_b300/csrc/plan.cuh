@@ -38,4 +38,44 @@ MLA_DEVI int worker_of(int64_t x, int64_t T, int G) {
   return (int)(g < G - 1 ? g : G - 1);
 }
 
+// Exclusive prefix of tiles_of(effective_len(b)) over b into pre[0..B]
+// (shared memory); every thread of the block takes part.  Invalid lengths
+// are reported once, by the thread that scans them.
+MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* status, int* pre) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int per = (B + nthr - 1) / nthr;
+  const int b0 = tid * per, b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += tiles_of(effective_len(seqlens, b, cap, status));
+  __shared__ int warp_sums[32];
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int warp_off = 0;
+  for (int w = 0; w < warp; ++w) warp_off += warp_sums[w];
+  int run = warp_off + incl - local;
+  for (int b = b0; b < b1; ++b) {
+    pre[b] = run;
+    run += tiles_of(effective_len(seqlens, b, cap, nullptr));
+  }
+  if (tid == nthr - 1) pre[B] = run;  // the last thread's running sum is the total
+  __syncthreads();
+}
+
+// The sequence owning tile x: the largest b with pre[b] <= x.
+MLA_DEVI int seq_of_tile(const int* pre, int B, int64_t x) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 }  // namespace mla

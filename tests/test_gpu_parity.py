@@ -367,3 +367,74 @@ def test_full_size_v3_step(mla):
         zr, _ = orc.decode_latent(q_ref[b], rows, wl.scale, wl.d_latent)
         o_ref.append(orc.out_proj(zr[None], w_uv)[0])
     assert_close(og[0::5], np.stack(o_ref), "o (full step)", mean_rel=6e-3)
+
+
+# ---------------------------------------------------------------- tensor-core decode (128 heads, d_c 512, d_R 64)
+TC_LENS = [0, 1, 63, 64, 65, 127, 128, 129, 191, 4097]
+
+
+@pytest.mark.parametrize("workers", [0, 1, 2, 5, 40, 300])
+def test_tc_decode_ragged_lengths(mla, workers):
+    """Every tail length, an empty sequence, and more split-KV workers than
+    tiles (idle CTA pairs); slack and unused blocks are NaN-poisoned."""
+    wl = mi.make_random(2001, 128, 512, 64, TC_LENS, paged=True)
+    z, lse, st = run_decode(mla, wl, num_workers=workers)
+    assert st == 0
+    check_decode(wl, z, lse)
+
+
+def test_tc_decode_contiguous_ragged(mla):
+    wl = mi.make_random(2002, 128, 512, 64, [4096, 1, 333, 0, 2049], paged=False)
+    for workers in (0, 3):
+        z, lse, st = run_decode(mla, wl, num_workers=workers)
+        assert st == 0
+        check_decode(wl, z, lse)
+
+
+def test_tc_and_generic_paths_agree_with_the_oracle(mla):
+    wl = mi.make_random(2003, 128, 512, 64, [700, 2048, 65], paged=True)
+    zt, lt, s1 = run_decode(mla, wl)
+    zg, lg, s2 = run_decode(mla, wl, flags=1)   # MLA_DECODE_FORCE_GENERIC
+    assert s1 == 0 and s2 == 0
+    check_decode(wl, zt, lt)
+    check_decode(wl, zg, lg)
+
+
+def test_tc_zero_query_gives_the_mean_of_visible_rows(mla):
+    wl = mi.make_random(2004, 128, 512, 64, [1, 63, 64, 65, 300], paged=True)
+    wl.q = np.zeros_like(wl.q)
+    z, lse, st = run_decode(mla, wl, num_workers=3)
+    assert st == 0
+    for b, L in enumerate(wl.seqlens):
+        rows = orc.gather_rows(wl.pool, b, int(L), wl.block_table, 64, 0)
+        want = rows[:, :wl.d_latent].mean(0)
+        assert np.allclose(z[b], want[None, :], rtol=0, atol=1e-5 * max(1.0, np.abs(want).max()))
+        assert np.allclose(lse[b], math.log(L), atol=1e-5)
+
+
+def test_tc_growing_scores_trigger_rescaling(mla):
+    """Cache rows whose magnitude grows along the sequence make the running
+    maximum climb tile after tile, so the output is rescaled many times."""
+    wl = mi.make_random(2005, 128, 512, 64, [3000, 1500], paged=False)
+    pool = orc.bf16_to_f64(wl.pool)
+    grow = (1.0 + np.arange(pool.shape[1]) / 256.0)[None, :, None]
+    wl.pool = orc.round_bf16_bits(np.where(np.isnan(pool), 0.0, pool) * grow)
+    for workers in (0, 1):
+        z, lse, st = run_decode(mla, wl, num_workers=workers)
+        assert st == 0
+        check_decode(wl, z, lse)
+
+
+def test_tc_out_of_range_inputs_are_reported_not_read(mla):
+    wl = mi.make_random(2006, 128, 512, 64, [100, 200, 50], paged=True)
+    sl = wl.seqlens.copy()
+    sl[1] = wl.max_blocks * 64 + 1
+    z, lse, st = run_decode(mla, wl, seqlens=sl)
+    assert st == 6 and np.all(z[1] == 0) and np.all(np.isneginf(lse[1]))
+    q64 = orc.bf16_to_f64(wl.q)
+    zs, _ = oracle_decode(wl, q64, wl.pool, wl.seqlens, batches=[0, 2])
+    assert_close(np.stack([z[0], z[2]]), np.stack([zs[0], zs[2]]), "z other sequences")
+    bt = wl.block_table.copy()
+    bt[0, 0] = wl.num_blocks + 5
+    z, lse, st = run_decode(mla, wl, block_table=i32(bt))
+    assert st == 6 and np.isfinite(z).all()
