@@ -46,15 +46,18 @@ bool dims_basic_ok(const mla_dims* d) {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t off_o, off_lse, total;
+  size_t off_o, off_lse, off_l, total;
 };
 
+// Workspace: per split-KV partial slot (worker g + sequence b) the latent
+// vector o [n_h][d_c] and two per-head scalars.
 WsLayout ws_layout(const mla_dims& d, int batch, int workers) {
   WsLayout w;
   const size_t slots = (size_t)workers + (size_t)batch;
   w.off_o = 256;
   w.off_lse = w.off_o + align256(slots * d.n_heads * d.d_latent * sizeof(float));
-  w.total = w.off_lse + align256(slots * d.n_heads * sizeof(float));
+  w.off_l = w.off_lse + align256(slots * d.n_heads * sizeof(float));
+  w.total = w.off_l + align256(slots * d.n_heads * sizeof(float));
   return w;
 }
 
@@ -185,12 +188,14 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.workers = G;
   a.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_o);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse);
+  a.l_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_l);
   a.z_out = z_out;
   a.z_is_fp32 = z_is_fp32 ? 1 : 0;
   a.lse_out = lse_out;
   a.status = dev_status;
   cudaStream_t s = as_stream(stream);
-  cudaError_t e = use_tc ? mla::launch_decode_tc(a, s) : mla::launch_decode_generic(a, sms, s);
+  if (use_tc) return from_cuda(mla::launch_decode_tc(a, s));  // partial pass + its combine
+  cudaError_t e = mla::launch_decode_generic(a, sms, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return from_cuda(mla::launch_combine(a, s));
 }

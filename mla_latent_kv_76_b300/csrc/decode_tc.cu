@@ -7,36 +7,31 @@
 //   s_j = scale * [q~_i ; q^R_i] . [c_j ; k^R_j],   z_i = sum_j softmax(s)_j c_j.
 //
 // Decomposition.  The fp32 accumulator O = 128 heads x 512 latent fills the
-// whole tensor memory of one SM, so a pair of CTAs (a cluster of two, one
-// per SM) shares every 64-token tile:
-//   CTA r owns latent columns [256 r, 256 r + 256) of O and of the score
-//   contraction; CTA 1 also owns the 64 RoPE columns.  Each CTA TMA-loads
-//   only its columns of the tile (every cache byte leaves HBM once), computes
-//   its partial score S_r = Q[:, cols_r] . C[:, cols_r]^T on the tensor core,
-//   and the two partials are swapped through distributed shared memory, so
-//   both CTAs hold the same S = S_0 + S_1 (fp32 addition commutes: the two
-//   copies are bitwise equal) and run the same online softmax.  Each then
-//   accumulates O[:, 256 r : 256 r + 256] += P . C[:, 256 r : 256 r + 256].
+// whole tensor memory of one SM, so each 128-token tile is shared by the two
+// CTAs of a cluster (one per SM), split by contraction rather than by columns:
+//   score CTA (rank 0)  S = [q~; q^R] . [c; k^R]^T over all 576 columns,
+//                       M = 128 heads x N = 128 tokens per tcgen05.mma, with
+//                       the query held in TMEM; online softmax; the bf16
+//                       weights P go to the peer through distributed shared
+//                       memory (16 KB per 64 tokens, the only exchange).
+//   value CTA (rank 1)  O += P . C[:, 0:512] (M = 128, N = 256, K = 64 tokens
+//                       per half tile), the whole accumulator in TMEM.
+// Every cache byte is read from HBM once by the score CTA; the value CTA
+// re-reads the latent columns a few microseconds later, from L2.
 //
-// Per CTA (256 threads):
-//   warp 0      TMA producer: one 64x64 bf16 box per 64-column chunk, three
-//               40 KB stages, 128-byte swizzle (the canonical K-major layout
-//               of the score MMA and the MN-major layout of the value MMA)
-//   warp 1      tcgen05.mma issuer (single thread) and TMEM owner
-//   warps 2-3   zero the rows past the sequence end in the last tile (NaN
-//               garbage in block slack must not meet a zero weight in the MMA);
-//               they see every fill of every stage and release it too
-//   warps 4-7   one thread per head: load Q, exchange the partial score,
-//               online softmax, write P (bf16) for the value MMA, rescale O
-//               when the running maximum grows, write the segment's partial
-// Tensor memory (512 columns x 128 lanes): O [0, 256), S double buffer
-// [256, 384), the CTA's Q columns as packed bf16 [384, 512) (A operand of
-// the score MMA read straight from TMEM).
+// Score CTA, 384 threads: warp 0 TMA (12 ring slots of 128 tokens x 64
+// columns, 128-byte swizzle), warp 1 MMA issue, warps 4-7 / 8-11 softmax for
+// token columns 0-63 / 64-127 (thread = head).
+// Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns), warp 1 MMA,
+// warps 2-3 zero the rows past the sequence end in the last half tile (NaN
+// garbage must not meet a zero weight), warps 4-7 rescale O and write the
+// segment's partial (thread = head), warp 8 returns P buffers to the score CTA.
 //
-// Online softmax with a lazily updated reference maximum: P = 2^(x - m_ref)
-// with x = s * scale * log2(e); m_ref moves (and O, l are rescaled) only when
-// a tile's maximum exceeds m_ref by more than 8, so P <= 256 and O never
-// overflows; the result is exact after the final division by l.
+// Online softmax with a lazily updated reference maximum m_ref (base 2):
+// P = 2^(x - m_ref); m_ref moves, and O and l are rescaled, only when a tile's
+// maximum exceeds m_ref by more than kRescaleThreshold.  The partial of a
+// segment is O unnormalised plus (m_ref, l); the combine kernel merges
+// partials exactly.
 #include <cuda.h>
 #include <mutex>
 
@@ -49,27 +44,45 @@ namespace mla {
 namespace {
 
 constexpr int kH = 128, kDC = 512, kD = 576;
-constexpr int kStages = 3;
-constexpr int kChunkBytes = 64 * 128;           // 64 tokens x 64 bf16, one 128-byte row per token
-constexpr int kStageBytes = 5 * kChunkBytes;    // up to 5 chunks per CTA (CTA 1: 4 latent + RoPE)
-constexpr int kQropeBytes = kH * 128;           // RoPE part of Q, 128 heads x 64 bf16
-constexpr int kPBytes = kH * 128;               // P, 128 heads x 64 tokens bf16
-constexpr int kRecvBytes = kH * 64 * 4;         // partial score from the peer, fp32
-constexpr int kOffStage = 0;
-constexpr int kOffQrope = kOffStage + kStages * kStageBytes;
-constexpr int kOffP = kOffQrope + kQropeBytes;
-constexpr int kOffRecv = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffRecv + kRecvBytes;
-constexpr int kNumBars = 21;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffPrefix = kOffMisc + 16;
+constexpr int kTile = 128;           // tokens per score tile (two 64-token halves)
+constexpr int kThreads = 384;
 constexpr int kTcMaxBatch = 1024;
-constexpr int kThreads = 256;
+constexpr float kRescaleThreshold = 16.f;
 
-// TMEM column map
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
+// ---- score CTA shared memory
+constexpr int kSlots = 12;
+constexpr int kSlotBytes = kTile * 128;            // 128 tokens x 64 bf16 columns
+constexpr int kOffRing = 0;
+constexpr int kOffXmax = kOffRing + kSlots * kSlotBytes;   // [2 parity][2 wg][128] fp32
+constexpr int kOffLsum = kOffXmax + 2 * 2 * kH * 4;        // [128] fp32
+// ---- value CTA shared memory
+constexpr int kVStages = 2;
+constexpr int kChunkBytes = 64 * 128;              // 64 tokens x 64 bf16 columns
+constexpr int kVStageBytes = 8 * kChunkBytes;      // the 512 latent columns of 64 tokens
+constexpr int kPBufs = 4;
+constexpr int kPBytes = kH * 128;                  // 128 heads x 64 tokens bf16
+constexpr int kMetaBytes = 1024;                   // alpha[128] fp32, flag[4] int32
+constexpr int kOffStage = 0;
+constexpr int kOffP = kOffStage + kVStages * kVStageBytes;
+constexpr int kOffMeta = kOffP + kPBufs * kPBytes;
+// ---- common tail
+constexpr int kOffBar = (kOffLsum + kH * 4 > kOffMeta + kPBufs * kMetaBytes) ? kOffLsum + kH * 4
+                                                                             : kOffMeta + kPBufs * kMetaBytes;
+constexpr int kNumBars = 40;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, event descriptor
+constexpr int kOffPrefix = kOffMisc + 32;
 
-constexpr float kRescaleThreshold = 8.f;  // log2 units
+// score CTA barriers
+constexpr int kBarCfull = 0, kBarCempty = 12, kBarSfull = 24, kBarSfree = 25, kBarQready = 26, kBarPfree = 27,
+              kBarScDrained = 31, kBarXmax = 32, kBarLsum = 34;
+// value CTA barriers
+constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOdone = 10, kBarOcomp = 14, kBarEvt = 15,
+              kBarEvtdone = 16, kBarVcDrained = 17;
+
+// TMEM columns
+constexpr uint32_t kColS = 0, kColQ = 128;  // score CTA (S: 128 tokens, Q: 576 bf16 packed in 288 columns)
+
+enum { kEvtRescale = 1, kEvtEpilogue = 2, kEvtExit = 3 };
 
 size_t tc_smem_bytes(int batch) { return (size_t)kOffPrefix + (size_t)(batch + 1) * 4 + 1024; }
 
@@ -84,12 +97,12 @@ struct TcParams {
   int32_t paged;
   float scale_log2;
   int32_t workers;  // CTA pairs
-  float* o_part;    // [(G + B)][128][512]
-  float* lse_part;  // [(G + B)][128]
+  float* o_part;    // [(G + B)][128][512]  unnormalised
+  float* m_part;    // [(G + B)][128]       reference maximum, log2 units
+  float* l_part;    // [(G + B)][128]       sum of weights relative to m_part
   int32_t* status;
 };
 
-// One segment of a worker's tile range: tiles [t_begin, t_begin + ntile) of sequence b.
 struct Seg {
   int b, t_begin, ntile, len;
 };
@@ -104,10 +117,21 @@ MLA_DEVI Seg seg_at(const int* pre, int B, int64_t x, int64_t hi, const TcParams
   return s;
 }
 
-// The last tile of a sequence whose length is not a multiple of 64 has rows
-// past the end that must be zeroed before the value MMA.
-MLA_DEVI bool is_tail(const Seg& s, int j) {
-  return (s.len & 63) != 0 && s.t_begin + j == tiles_of(s.len) - 1;
+// 64-token halves of tile tt that hold visible tokens (1 or 2).
+MLA_DEVI int halves_of(const Seg& s, int tt) { return min(2, (s.len - tt * kTile + 63) >> 6); }
+
+// Does half w of tile tt contain the sequence end with a partial block?
+MLA_DEVI bool half_is_tail(const Seg& s, int tt, int w) {
+  const int lo = tt * kTile + 64 * w;
+  return (s.len & 63) != 0 && lo <= s.len - 1 && s.len - 1 < lo + 64;
+}
+
+// Paged block id of half w of tile tt, or -1 if it is out of range.
+MLA_DEVI int half_block(const TcParams& p, const Seg& s, int tt, int w) {
+  const int lb = 2 * tt + w;
+  if (lb >= p.max_blocks) return -1;
+  const int blk = p.block_table[(int64_t)s.b * p.max_blocks + lb];
+  return (blk >= 0 && blk < p.num_blocks) ? blk : -1;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -115,53 +139,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint64_t* full = bars + 0;      // [3] TMA landed (count 1 + tx)
-  // [3] stage free again: the value MMA's commit plus the 64 tail-zeroing
-  // threads, which therefore see every fill of every stage in order
-  uint64_t* empty = bars + 3;
-  uint64_t* sfull = bars + 6;     // [2] score MMA done (commit)
-  uint64_t* sfree = bars + 8;     // [2] score read out of TMEM (128)
-  uint64_t* pfull = bars + 10;    // [2] P written (128)
-  uint64_t* odone = bars + 12;    // value MMA of a tile done (commit)
-  uint64_t* ofree = bars + 13;    // O read out at a segment end (128)
-  uint64_t* qready = bars + 14;   // Q of the segment in TMEM / smem (128)
-  uint64_t* recvfull = bars + 15; // the peer's partial score arrived (128 remote)
-  uint64_t* peerfree = bars + 16; // the peer consumed what this CTA sent (128 remote)
-  uint64_t* drained = bars + 17;  // all MMAs of this CTA done (commit, at exit)
-  // [3] tail rows of the stage zeroed (64).  One per stage: a stage cannot be
-  // refilled before the MMA has consumed its tail, so no phase is ever skipped.
-  uint64_t* fixdone = bars + 18;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(sm + kOffMisc + 4);
+  volatile int* evt_desc = reinterpret_cast<volatile int*>(sm + kOffMisc + 8);  // type, buffer, slot
   int* pre = reinterpret_cast<int*>(sm + kOffPrefix);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
+  const uint32_t rank = tc::cluster_rank();
   const int g = (int)(blockIdx.x >> 1);
-  const int64_t cap = p.paged ? (int64_t)p.max_blocks * kTileTokens : p.seq_stride;
+  const int64_t cap = p.paged ? (int64_t)p.max_blocks * 64 : p.seq_stride;
 
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1 + 64);
+    if (rank == 0) {
+      for (int i = 0; i < kSlots; ++i) {
+        tc::mbar_init(&bars[kBarCfull + i], 1);
+        tc::mbar_init(&bars[kBarCempty + i], 1);
+      }
+      tc::mbar_init(&bars[kBarSfull], 1);
+      tc::mbar_init(&bars[kBarSfree], 256);
+      tc::mbar_init(&bars[kBarQready], 256);
+      for (int i = 0; i < kPBufs; ++i) tc::mbar_init(&bars[kBarPfree + i], 1);
+      tc::mbar_init(&bars[kBarScDrained], 1);
+      tc::mbar_init(&bars[kBarXmax], 256);
+      tc::mbar_init(&bars[kBarXmax + 1], 256);
+      tc::mbar_init(&bars[kBarLsum], 256);
+    } else {
+      for (int i = 0; i < kVStages; ++i) {
+        tc::mbar_init(&bars[kBarFull + i], 1);
+        tc::mbar_init(&bars[kBarEmpty + i], 1 + 64);
+        tc::mbar_init(&bars[kBarFix + i], 64);
+      }
+      for (int i = 0; i < kPBufs; ++i) {
+        tc::mbar_init(&bars[kBarPfull + i], 128);
+        tc::mbar_init(&bars[kBarOdone + i], 1);
+      }
+      tc::mbar_init(&bars[kBarOcomp], 1);
+      tc::mbar_init(&bars[kBarEvt], 1);
+      tc::mbar_init(&bars[kBarEvtdone], 128);
+      tc::mbar_init(&bars[kBarVcDrained], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sfull[i], 1);
-      tc::mbar_init(&sfree[i], 128);
-      tc::mbar_init(&pfull[i], 128);
-    }
-    tc::mbar_init(odone, 1);
-    tc::mbar_init(ofree, 128);
-    tc::mbar_init(qready, 128);
-    for (int i = 0; i < 3; ++i) tc::mbar_init(&fixdone[i], 64);
-    tc::mbar_init(recvfull, 128);
-    tc::mbar_init(peerfree, 128);
-    tc::mbar_init(drained, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
-  tile_prefix(p.seqlens, p.batch, cap, p.status, pre);  // ends with __syncthreads
+  tile_prefix(p.seqlens, p.batch, cap, p.status, pre, kTile);  // ends with __syncthreads
   tc::tc_fence_before();
   tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival
   tc::tc_fence_after();
@@ -171,296 +192,436 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int B = p.batch, G = p.workers;
   const int64_t T = pre[B];
   const int64_t lo = worker_begin(g, T, G), hi = worker_begin(g + 1, T, G);
-  const int chunk0 = (int)rank * 4;
-  const int nchunk = rank ? 5 : 4;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tc::prefetch_map(&cache_map);
-      int n = 0;
-      bool ok = true;
-      for (int64_t x = lo; x < hi && ok;) {
-        const Seg s = seg_at(pre, B, x, hi, p, cap);
-        x += s.ntile;
-        for (int j = 0; j < s.ntile; ++j, ++n) {
-          const int st = n % kStages;
-          if (n >= kStages && !tc::wait<false>(&empty[st], ((n / kStages) - 1) & 1, ab)) {
-            ok = false;
-            break;
-          }
-          uint8_t* dst = sm + kOffStage + st * kStageBytes;
-          const int tt = s.t_begin + j;
-          if (p.paged) {
-            const int blk = p.block_table[(int64_t)s.b * p.max_blocks + tt];
-            if (blk < 0 || blk >= p.num_blocks) {
-              // unreadable block: its rows count as zeros
-              report(p.status, MLA_ERR_DEVICE_BOUNDS);
-              uint4* z = reinterpret_cast<uint4*>(dst);
-              for (int i = 0; i < nchunk * kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-              tc::fence_async_smem();
-              tc::mbar_arrive(&full[st]);
-              continue;
+  if (rank == 0) {
+    // ================================================================ score CTA
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        tc::prefetch_map(&cache_map);
+        int n = 0;  // chunk counter: 9 per tile
+        bool ok = true;
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j) {
+            const int tt = s.t_begin + j;
+            const int nh = halves_of(s, tt);
+            int blk[2] = {-1, -1};
+            int nvalid = nh;
+            if (p.paged) {
+              nvalid = 0;
+              for (int w = 0; w < nh; ++w) {
+                blk[w] = half_block(p, s, tt, w);
+                if (blk[w] < 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
+                else ++nvalid;
+              }
             }
-            tc::mbar_expect_tx(&full[st], nchunk * kChunkBytes);
-            for (int c = 0; c < nchunk; ++c)
-              tc::tma_load_3d(dst + c * kChunkBytes, &cache_map, (chunk0 + c) * 64, 0, blk, &full[st]);
-          } else {
-            tc::mbar_expect_tx(&full[st], nchunk * kChunkBytes);
-            for (int c = 0; c < nchunk; ++c)
-              tc::tma_load_3d(dst + c * kChunkBytes, &cache_map, (chunk0 + c) * 64, tt * 64, s.b, &full[st]);
+            for (int c = 0; c < 9; ++c, ++n) {
+              const int sl = n % kSlots, u = n / kSlots;
+              if (u >= 1 && !tc::wait<false>(&bars[kBarCempty + sl], (u - 1) & 1, ab)) {
+                ok = false;
+                break;
+              }
+              uint8_t* dst = sm + kOffRing + sl * kSlotBytes;
+              uint64_t* fb = &bars[kBarCfull + sl];
+              if (p.paged && nvalid < nh) {  // unreadable block: its rows count as zeros
+                for (int w = 0; w < nh; ++w)
+                  if (blk[w] < 0) {
+                    uint4* z = reinterpret_cast<uint4*>(dst + w * kChunkBytes);
+                    for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                  }
+                tc::fence_async_smem();
+              }
+              if (nvalid == 0) {
+                tc::mbar_arrive(fb);
+                continue;
+              }
+              tc::mbar_expect_tx(fb, nvalid * kChunkBytes);
+              for (int w = 0; w < nh; ++w) {
+                if (p.paged) {
+                  if (blk[w] >= 0) tc::tma_load_3d(dst + w * kChunkBytes, &cache_map, c * 64, 0, blk[w], fb);
+                } else {
+                  tc::tma_load_3d(dst + w * kChunkBytes, &cache_map, c * 64, tt * kTile + 64 * w, s.b, fb);
+                }
+              }
+            }
           }
         }
-      }
-      // never leave with a copy in flight: wait for the last use of every stage
-      for (int k = 1; k <= kStages && k <= n; ++k) {
-        const int m = n - k;
-        tc::wait<false>(&full[m % kStages], (m / kStages) & 1, ab);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);
-      constexpr uint32_t idO = tc::idesc_bf16(128, 256, 0, 1);
-      const uint32_t sbase = smem_u32(sm + kOffStage);
-      const uint32_t qrope = smem_u32(sm + kOffQrope);
-      const uint32_t pbase = smem_u32(sm + kOffP);
-      int n = 0, seg_i = 0;
-      int ntail[kStages] = {0, 0, 0};
-      bool ok = true;
-      auto issue_o = [&](int m, bool first_in_seg) -> bool {
-        if (!tc::wait<false>(&pfull[m & 1], (m >> 1) & 1, ab)) return false;
-        if (first_in_seg && seg_i > 0 && !tc::wait<false>(ofree, (seg_i - 1) & 1, ab)) return false;
-        tc::tc_fence_after();
-        const uint32_t stg = sbase + (m % kStages) * kStageBytes;
-        const uint32_t pb = pbase + (m & 1) * kPBytes;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_ss(tb + kColO, tc::smem_desc(pb + k * 32, 16, 1024), tc::smem_desc(stg + k * 2048, kChunkBytes, 1024),
-                     idO, (first_in_seg && k == 0) ? 0u : 1u);
-        tc::mma_commit(&empty[m % kStages]);
-        tc::mma_commit(odone);
-        return true;
-      };
-      for (int64_t x = lo; x < hi && ok;) {
-        const Seg s = seg_at(pre, B, x, hi, p, cap);
-        x += s.ntile;
-        if (!tc::wait<false>(qready, seg_i & 1, ab)) break;
-        tc::tc_fence_after();
-        for (int j = 0; j < s.ntile; ++j) {
-          const int m = n + j;
-          const int st = m % kStages;
-          if (!tc::wait<false>(&full[st], (m / kStages) & 1, ab)) { ok = false; break; }
-          if (is_tail(s, j)) {
-            if (!tc::wait<false>(&fixdone[st], ntail[st] & 1, ab)) { ok = false; break; }
-            ++ntail[st];
-          }
-          if (m >= 2 && !tc::wait<false>(&sfree[m & 1], ((m >> 1) - 1) & 1, ab)) { ok = false; break; }
-          tc::tc_fence_after();
-          const uint32_t stg = sbase + st * kStageBytes;
-          const uint32_t dS = tb + kColS + (m & 1) * 64;
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            tc::mma_ts(dS, tb + kColQ + k * 8, tc::smem_desc(stg + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
-                       idS, k > 0 ? 1u : 0u);
-          if (rank == 1) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tc::mma_ss(dS, tc::smem_desc(qrope + k * 32, 16, 1024),
-                         tc::smem_desc(stg + 4 * kChunkBytes + k * 32, 16, 1024), idS, 1u);
-          }
-          tc::mma_commit(&sfull[m & 1]);
-          if (j >= 1 && !issue_o(m - 1, j == 1)) { ok = false; break; }
+        for (int k = 1; k <= kSlots && k <= n; ++k) {  // no copy in flight at exit
+          const int m = n - k;
+          tc::wait<false>(&bars[kBarCfull + m % kSlots], (m / kSlots) & 1, ab);
         }
-        if (!ok) break;
-        if (!issue_o(n + s.ntile - 1, s.ntile == 1)) break;
-        n += s.ntile;
-        ++seg_i;
       }
-      // drain: nothing may still read or write TMEM / shared memory at exit
-      tc::mma_commit(drained);
-      tc::wait<false>(drained, 0, ab);
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ tail zeroing
-    const int t = tid - 64;  // 0..63
-    int n = 0;
-    bool ok = true;
-    for (int64_t x = lo; x < hi && ok;) {
-      const Seg s = seg_at(pre, B, x, hi, p, cap);
-      x += s.ntile;
-      for (int j = 0; j < s.ntile; ++j) {
-        const int m = n + j;
-        if (!tc::wait<false>(&full[m % kStages], (m / kStages) & 1, ab)) { ok = false; break; }
-        if (is_tail(s, j)) {
-          uint8_t* stg = sm + kOffStage + (m % kStages) * kStageBytes;
-          const int r0 = s.len & 63;
-          const int per_chunk = (64 - r0) * 8;  // 16-byte pieces per chunk
-          for (int i = t; i < 4 * per_chunk; i += 64) {
-            const int c = i / per_chunk, k = i % per_chunk;
-            *reinterpret_cast<uint4*>(stg + c * kChunkBytes + (r0 + (k >> 3)) * 128 + (k & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- score MMA
+        constexpr uint32_t idS = tc::idesc_bf16(128, kTile, 0, 0);
+        const uint32_t ring = smem_u32(sm + kOffRing);
+        int n = 0, m = 0, k = 0;
+        bool ok = true;
+        for (int64_t x = lo; x < hi && ok; ++k) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          if (!tc::wait<false>(&bars[kBarQready], k & 1, ab)) break;
+          for (int j = 0; j < s.ntile && ok; ++j, ++m) {
+            if (m >= 1 && !tc::wait<false>(&bars[kBarSfree], (m - 1) & 1, ab)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            for (int c = 0; c < 9; ++c, ++n) {
+              const int sl = n % kSlots;
+              if (!tc::wait<false>(&bars[kBarCfull + sl], (n / kSlots) & 1, ab)) {
+                ok = false;
+                break;
+              }
+              tc::tc_fence_after();
+              const uint32_t sa = ring + sl * kSlotBytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc::mma_ts(tb + kColS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
+                           (c | kk) != 0 ? 1u : 0u);
+              tc::mma_commit(&bars[kBarCempty + sl]);
+            }
+            if (ok) tc::mma_commit(&bars[kBarSfull]);
           }
-          tc::fence_async_smem();
-          tc::mbar_arrive(&fixdone[m % kStages]);
         }
-        tc::mbar_arrive(&empty[m % kStages]);
+        tc::mma_commit(&bars[kBarScDrained]);
+        tc::wait<false>(&bars[kBarScDrained], 0, ab);
       }
-      n += s.ntile;
-    }
-  } else {
-    // ------------------------------------------------------------ softmax (thread = head)
-    const int h = tid - 128;
-    const int wq = warp - 4;
-    const uint32_t lane_t = tb + ((uint32_t)(wq * 32) << 16);
-    const float4* recv = reinterpret_cast<const float4*>(sm + kOffRecv);
-    const uint32_t peer_recv = tc::map_peer(sm + kOffRecv, peer) + (uint32_t)h * 16u;
-    uint8_t* qrope_s = sm + kOffQrope;
+    } else if (warp >= 4) {
+      // ------------------------------------------------------------ softmax (thread = head)
+      const int w = (warp - 4) >> 2;  // token columns [64 w, 64 w + 64) of each tile
+      const int h = (tid - 128) & 127;
+      const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
+      float* xmax = reinterpret_cast<float*>(sm + kOffXmax);
+      float* lsum = reinterpret_cast<float*>(sm + kOffLsum);
+      // the value CTA's P buffers, metadata and arrival barriers
+      const uint32_t r_p = tc::map_peer(sm + kOffP, 1);
+      const uint32_t r_meta = tc::map_peer(sm + kOffMeta, 1);
+      const uint32_t r_pfull = tc::map_peer(&bars[kBarPfull], 1);
 
-    auto load_q = [&](int b) {
-      const __nv_bfloat16* row = p.q + ((int64_t)b * kH + h) * kD;
-      const uint4* src = reinterpret_cast<const uint4*>(row + rank * 256);
+      auto load_q = [&](int b) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * kH + h) * kD + 288 * w);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = __ldg(src + c * 8 + i);
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+          }
+          tc::tmem_st32(lane_t + kColQ + 144 * w + c * 32, r);
+        }
+        uint32_t r[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(src + c * 8 + i);
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = __ldg(src + 32 + i);
           r[4 * i] = v.x;
           r[4 * i + 1] = v.y;
           r[4 * i + 2] = v.z;
           r[4 * i + 3] = v.w;
         }
-        tc::tmem_st32(lane_t + kColQ + c * 32, r);
-      }
-      if (rank == 1) {
-        const uint4* srcr = reinterpret_cast<const uint4*>(row + kDC);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(qrope_s + h * 128 + ((c ^ (h & 7)) * 16)) = __ldg(srcr + c);
-      }
-      tc::tmem_wait_st();
-      tc::fence_async_smem();
-      tc::tc_fence_before();
-      tc::mbar_arrive(qready);
-    };
-
-    int n = 0;
-    bool ok = true;
-    bool first_seg = true;
-    for (int64_t x = lo; x < hi && ok;) {
-      const Seg s = seg_at(pre, B, x, hi, p, cap);
-      x += s.ntile;
-      if (first_seg) load_q(s.b);
-      first_seg = false;
-      float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < s.ntile; ++j) {
-        const int m = n + j;
-        if (!tc::wait<false>(&sfull[m & 1], (m >> 1) & 1, ab)) { ok = false; break; }
-        tc::tc_fence_after();
-        uint32_t sa[32], sb[32];
-        tc::tmem_ld32(lane_t + kColS + (m & 1) * 64, sa);
-        tc::tmem_ld32(lane_t + kColS + (m & 1) * 64 + 32, sb);
-        tc::tmem_wait_ld();
+        tc::tmem_st16(lane_t + kColQ + 144 * w + 128, r);
+        tc::tmem_wait_st();
         tc::tc_fence_before();
-        tc::mbar_arrive(&sfree[m & 1]);
-        // ---- swap partial scores with the peer CTA
-        if (m >= 1 && !tc::wait<true>(peerfree, (m - 1) & 1, ab)) { ok = false; break; }
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-          tc::st_cluster_v4(peer_recv + c4 * kH * 16, __uint_as_float(sa[4 * c4]), __uint_as_float(sa[4 * c4 + 1]),
-                            __uint_as_float(sa[4 * c4 + 2]), __uint_as_float(sa[4 * c4 + 3]));
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-          tc::st_cluster_v4(peer_recv + (8 + c4) * kH * 16, __uint_as_float(sb[4 * c4]),
-                            __uint_as_float(sb[4 * c4 + 1]), __uint_as_float(sb[4 * c4 + 2]),
-                            __uint_as_float(sb[4 * c4 + 3]));
-        tc::mbar_arrive_remote(recvfull, peer);
-        if (!tc::wait<true>(recvfull, m & 1, ab)) { ok = false; break; }
-        float x64[64];
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 v = recv[c4 * kH + h];
-          const uint32_t* own = c4 < 8 ? &sa[4 * c4] : &sb[4 * (c4 - 8)];
-          x64[4 * c4 + 0] = __uint_as_float(own[0]) + v.x;
-          x64[4 * c4 + 1] = __uint_as_float(own[1]) + v.y;
-          x64[4 * c4 + 2] = __uint_as_float(own[2]) + v.z;
-          x64[4 * c4 + 3] = __uint_as_float(own[3]) + v.w;
-        }
-        tc::mbar_arrive_remote(peerfree, peer);
-        // ---- scale, mask, tile maximum
-        const int nvalid = s.len - (s.t_begin + j) * 64;  // >= 1
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x64[c] = (c < nvalid) ? x64[c] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x64[c]);
-        }
-        if (j >= 1) {
-          if (!tc::wait<false>(odone, (m - 1) & 1, ab)) { ok = false; break; }
-          tc::tc_fence_after();
-        }
-        // TMEM loads / stores are warp-collective: the warp rescales together,
-        // heads that keep their reference maximum multiply by exactly 1
-        const bool grow = mt > m_ref + kRescaleThreshold;
-        const bool rescaled = __any_sync(0xffffffffu, grow && j >= 1);
-        if (rescaled) {
-          const float f = (grow && j >= 1) ? exp2f(m_ref - mt) : 1.f;
-          l *= f;
-#pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            uint32_t r[32];
-            tc::tmem_ld32(lane_t + kColO + c * 32, r);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-            tc::tmem_st32(lane_t + kColO + c * 32, r);
+        tc::mbar_arrive(&bars[kBarQready]);
+      };
+
+      int m = 0, hh = 0, k = 0;
+      bool ok = true, first = true;
+      for (int64_t x = lo; x < hi && ok; ++k) {
+        const Seg s = seg_at(pre, B, x, hi, p, cap);
+        x += s.ntile;
+        if (first) load_q(s.b);
+        first = false;
+        float m_ref = -INFINITY, l = 0.f;
+        for (int j = 0; j < s.ntile; ++j, ++m) {
+          const int tt = s.t_begin + j;
+          const int nh = halves_of(s, tt);
+          if (!tc::wait<false>(&bars[kBarSfull], m & 1, ab)) {
+            ok = false;
+            break;
           }
-        }
-        if (grow) m_ref = mt;
-        // ---- P = 2^(x - m_ref) in bf16; l sums the rounded weights
-        uint8_t* prow = sm + kOffP + (m & 1) * kPBytes + h * 128;
+          tc::tc_fence_after();
+          uint32_t sa[32], sb[32];
+          tc::tmem_ld32(lane_t + kColS + 64 * w, sa);
+          tc::tmem_ld32(lane_t + kColS + 64 * w + 32, sb);
+          tc::tmem_wait_ld();
+          tc::tc_fence_before();
+          tc::mbar_arrive(&bars[kBarSfree]);
+          const int nvalid = s.len - tt * kTile - 64 * w;  // may be <= 0
+          float xv[64];
+          float mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
+          for (int c = 0; c < 64; ++c) {
+            const float sv = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
+            xv[c] = (c < nvalid) ? sv * p.scale_log2 : -INFINITY;
+            mt = fmaxf(mt, xv[c]);
+          }
+          // tile maximum over both halves (bounded rendezvous of the two warpgroups)
+          float* xm = xmax + (m & 1) * 2 * kH;
+          xm[w * kH + h] = mt;
+          tc::mbar_arrive(&bars[kBarXmax + (m & 1)]);
+          if (!tc::wait<false>(&bars[kBarXmax + (m & 1)], (m >> 1) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          mt = fmaxf(xm[h], xm[kH + h]);
+          float alpha = 1.f;
+          if (j == 0) {
+            m_ref = mt;
+          } else if (mt > m_ref + kRescaleThreshold) {
+            alpha = exp2f(m_ref - mt);
+            l *= alpha;
+            m_ref = mt;
+          }
+          // P = 2^(x - m_ref) in bf16; l sums the rounded weights
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float p0 = exp2f(x64[8 * c + 2 * i] - m_ref);
-            const float p1 = exp2f(x64[8 * c + 2 * i + 1] - m_ref);
-            pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 32; ++i) {
+            pk[i] = pack_bf16x2(exp2f(xv[2 * i] - m_ref), exp2f(xv[2 * i + 1] - m_ref));
             l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
           }
-          *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        tc::fence_async_smem();
-        if (rescaled) tc::tmem_wait_st();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&pfull[m & 1]);
-      }
-      if (!ok) break;
-      n += s.ntile;
-      // the next segment's Q can go in as soon as this segment's last score is read
-      if (x < hi) load_q(seq_of_tile(pre, B, x));
-      // ---- segment result: O / l and the log-sum-exp
-      if (!tc::wait<false>(odone, (n - 1) & 1, ab)) break;
-      tc::tc_fence_after();
-      const float inv = 1.f / l;
-      float* dst = p.o_part + (((int64_t)g + s.b) * kH + h) * kDC + rank * 256;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(lane_t + kColO + c * 32, r);
-        tc::tmem_wait_ld();
+          if (w < nh) {
+            const int hidx = hh + w;
+            const int pb = hidx % kPBufs, u = hidx / kPBufs;
+            if (u >= 1 && !tc::wait<true>(&bars[kBarPfree + pb], (u - 1) & 1, ab)) {
+              ok = false;
+              break;
+            }
+            const uint32_t row = r_p + pb * kPBytes + h * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(dst + c * 32)[i] =
-              make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                          __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+            for (int c = 0; c < 8; ++c)
+              tc::st_cluster_u4(row + ((c ^ (h & 7)) * 16), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            const uint32_t meta = r_meta + pb * kMetaBytes;
+            const bool any = __any_sync(0xffffffffu, alpha != 1.f);
+            if (w == 0) tc::st_cluster_u32(meta + h * 4, __float_as_uint(alpha));
+            if (lane == 0) tc::st_cluster_u32(meta + 512 + (warp & 3) * 4, (w == 0 && any) ? 1u : 0u);
+            tc::mbar_arrive_cluster_addr(r_pfull + pb * 8);
+          }
+          hh += nh;
+        }
+        if (!ok) break;
+        // ---- segment end: (m_ref, l) of the partial, then the next segment's query
+        // (the next write of lsum comes a whole tile later, past a rendezvous with warpgroup 0)
+        if (w == 1) lsum[h] = l;
+        tc::mbar_arrive(&bars[kBarLsum]);
+        if (!tc::wait<false>(&bars[kBarLsum], k & 1, ab)) break;
+        if (w == 0) {
+          const int64_t slot = (int64_t)g + s.b;
+          p.m_part[slot * kH + h] = m_ref;
+          p.l_part[slot * kH + h] = l + lsum[h];
+        }
+        if (x < hi) load_q(seq_of_tile(pre, B, x));
       }
-      if (rank == 0) p.lse_part[((int64_t)g + s.b) * kH + h] = (m_ref + log2f(l)) * kLn2;
-      tc::tc_fence_before();
-      tc::mbar_arrive(ofree);
+    }
+  } else {
+    // ================================================================ value CTA
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        tc::prefetch_map(&cache_map);
+        int hh = 0;
+        bool ok = true;
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j) {
+            const int tt = s.t_begin + j;
+            const int nh = halves_of(s, tt);
+            for (int w = 0; w < nh; ++w, ++hh) {
+              const int st = hh % kVStages, u = hh / kVStages;
+              if (u >= 1 && !tc::wait<false>(&bars[kBarEmpty + st], (u - 1) & 1, ab)) {
+                ok = false;
+                break;
+              }
+              uint8_t* dst = sm + kOffStage + st * kVStageBytes;
+              uint64_t* fb = &bars[kBarFull + st];
+              if (p.paged) {
+                const int blk = half_block(p, s, tt, w);
+                if (blk < 0) {
+                  uint4* z = reinterpret_cast<uint4*>(dst);
+                  for (int i = 0; i < kVStageBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                  tc::fence_async_smem();
+                  tc::mbar_arrive(fb);
+                  continue;
+                }
+                tc::mbar_expect_tx(fb, kVStageBytes);
+                for (int c = 0; c < 8; ++c) tc::tma_load_3d(dst + c * kChunkBytes, &cache_map, c * 64, 0, blk, fb);
+              } else {
+                tc::mbar_expect_tx(fb, kVStageBytes);
+                for (int c = 0; c < 8; ++c)
+                  tc::tma_load_3d(dst + c * kChunkBytes, &cache_map, c * 64, tt * kTile + 64 * w, s.b, fb);
+              }
+            }
+          }
+        }
+        for (int k = 1; k <= kVStages && k <= hh; ++k) {
+          const int m = hh - k;
+          tc::wait<false>(&bars[kBarFull + m % kVStages], (m / kVStages) & 1, ab);
+        }
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- value MMA
+        constexpr uint32_t idO = tc::idesc_bf16(128, 256, 0, 1);
+        const uint32_t stg0 = smem_u32(sm + kOffStage);
+        const uint32_t pb0 = smem_u32(sm + kOffP);
+        const volatile int* meta_flags = reinterpret_cast<const volatile int*>(sm + kOffMeta + 512);
+        int hh = 0, oc = 0, ev = 0;
+        int ntail[kVStages] = {0, 0};
+        bool ok = true;
+        auto post = [&](int type, int a, int b2) -> bool {  // one event at a time
+          evt_desc[0] = type;
+          evt_desc[1] = a;
+          evt_desc[2] = b2;
+          tc::mbar_arrive(&bars[kBarEvt]);
+          ++ev;
+          return type == kEvtExit || tc::wait<false>(&bars[kBarEvtdone], (ev - 1) & 1, ab);
+        };
+        auto drain = [&]() -> bool {
+          tc::mma_commit(&bars[kBarOcomp]);
+          return tc::wait<false>(&bars[kBarOcomp], (oc++) & 1, ab);
+        };
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          bool first_half = true;
+          for (int j = 0; j < s.ntile && ok; ++j) {
+            const int tt = s.t_begin + j;
+            const int nh = halves_of(s, tt);
+            for (int w = 0; w < nh; ++w, ++hh) {
+              const int st = hh % kVStages, pb = hh % kPBufs;
+              if (!tc::wait<false>(&bars[kBarFull + st], (hh / kVStages) & 1, ab)) { ok = false; break; }
+              if (half_is_tail(s, tt, w)) {
+                if (!tc::wait<false>(&bars[kBarFix + st], ntail[st] & 1, ab)) { ok = false; break; }
+                ++ntail[st];
+              }
+              if (!tc::wait<true>(&bars[kBarPfull + pb], (hh / kPBufs) & 1, ab)) { ok = false; break; }
+              const volatile int* fl = meta_flags + pb * (kMetaBytes / 4);
+              if (fl[0] | fl[1] | fl[2] | fl[3]) {  // the reference maximum moved: rescale O first
+                if (!drain() || !post(kEvtRescale, pb, 0)) { ok = false; break; }
+              }
+              tc::tc_fence_after();
+              const uint32_t sa = stg0 + st * kVStageBytes, pa = pb0 + pb * kPBytes;
+#pragma unroll
+              for (int n2 = 0; n2 < 2; ++n2)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc::mma_ss(tb + n2 * 256, tc::smem_desc(pa + kk * 32, 16, 1024),
+                             tc::smem_desc(sa + n2 * 4 * kChunkBytes + kk * 2048, kChunkBytes, 1024), idO,
+                             (first_half && kk == 0) ? 0u : 1u);
+              tc::mma_commit(&bars[kBarEmpty + st]);
+              tc::mma_commit(&bars[kBarOdone + pb]);
+              first_half = false;
+            }
+          }
+          if (!ok) break;
+          // segment end: the partial's O goes out before the next segment overwrites it
+          if (!drain() || !post(kEvtEpilogue, 0, g + s.b)) break;
+        }
+        post(kEvtExit, 0, 0);
+        tc::mma_commit(&bars[kBarVcDrained]);
+        tc::wait<false>(&bars[kBarVcDrained], 0, ab);
+      }
+    } else if (warp < 4) {
+      // ------------------------------------------------------------ tail zeroing
+      const int t = tid - 64;
+      int hh = 0;
+      bool ok = true;
+      for (int64_t x = lo; x < hi && ok;) {
+        const Seg s = seg_at(pre, B, x, hi, p, cap);
+        x += s.ntile;
+        for (int j = 0; j < s.ntile && ok; ++j) {
+          const int tt = s.t_begin + j;
+          const int nh = halves_of(s, tt);
+          for (int w = 0; w < nh; ++w, ++hh) {
+            const int st = hh % kVStages;
+            if (!tc::wait<false>(&bars[kBarFull + st], (hh / kVStages) & 1, ab)) {
+              ok = false;
+              break;
+            }
+            if (half_is_tail(s, tt, w)) {
+              uint8_t* stg = sm + kOffStage + st * kVStageBytes;
+              const int r0 = s.len & 63;
+              const int per_chunk = (64 - r0) * 8;  // 16-byte pieces per chunk
+              for (int i = t; i < 8 * per_chunk; i += 64) {
+                const int c = i / per_chunk, k = i % per_chunk;
+                *reinterpret_cast<uint4*>(stg + c * kChunkBytes + (r0 + (k >> 3)) * 128 + (k & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+              tc::fence_async_smem();
+              tc::mbar_arrive(&bars[kBarFix + st]);
+            }
+            tc::mbar_arrive(&bars[kBarEmpty + st]);
+          }
+        }
+      }
+    } else if (warp < 8) {
+      // ------------------------------------------------------------ rescale / epilogue (thread = head)
+      const int h = tid - 128;
+      const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
+      for (int e = 0;; ++e) {
+        if (!tc::wait<false>(&bars[kBarEvt], e & 1, ab)) break;
+        tc::tc_fence_after();
+        const int type = evt_desc[0], arg = evt_desc[1], slot = evt_desc[2];
+        if (type == kEvtExit) break;
+        if (type == kEvtRescale) {
+          const float a = reinterpret_cast<const float*>(sm + kOffMeta + arg * kMetaBytes)[h];
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            uint32_t r[32];
+            tc::tmem_ld32(lane_t + c * 32, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+            tc::tmem_st32(lane_t + c * 32, r);
+          }
+          tc::tmem_wait_st();
+        } else {
+          float* dst = p.o_part + ((int64_t)slot * kH + h) * kDC;
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            uint32_t r[32];
+            tc::tmem_ld32(lane_t + c * 32, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              reinterpret_cast<float4*>(dst + c * 32)[i] =
+                  make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                              __uint_as_float(r[4 * i + 3]));
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[kBarEvtdone]);
+      }
+    } else if (warp == 8) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- P buffers back to the score CTA
+        const uint32_t r_pfree = tc::map_peer(sm + kOffBar + kBarPfree * 8, 0);
+        int hh = 0;
+        bool ok = true;
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j) {
+            const int nh = halves_of(s, s.t_begin + j);
+            for (int w = 0; w < nh; ++w, ++hh) {
+              const int pb = hh % kPBufs;
+              if (!tc::wait<false>(&bars[kBarOdone + pb], (hh / kPBufs) & 1, ab)) {
+                ok = false;
+                break;
+              }
+              tc::mbar_arrive_cluster_addr(r_pfree + pb * 8);
+            }
+          }
+        }
+      }
     }
   }
 
@@ -472,6 +633,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tb, 512);
   }
+}
+
+// ------------------------------------------------------------------ combine
+// Partials are unnormalised: O_s with reference maximum m_s (log2 units) and
+// weight sum l_s.  M = max_s m_s, L = sum_s l_s 2^(m_s - M),
+// z = sum_s 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.  One warp per head.
+template <bool ZF32>
+__global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 4 + warp;
+  const int G = a.workers;
+  const float* m_part = a.lse_part;
+  const float* l_part = a.l_part;
+  const int64_t cap = a.block_table ? (int64_t)a.max_blocks * 64 : a.seq_stride;
+  long long before = 0, total = 0;
+  for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+    const int t = tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile);
+    total += t;
+    if (i < b) before += t;
+  }
+  __shared__ long long red[2][4];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  if (lane == 0) {
+    red[0][warp] = before;
+    red[1][warp] = total;
+  }
+  __syncthreads();
+  const int64_t Sb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+  const int64_t T = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  if (h >= kH) return;
+  const int nb = tiles_of(effective_len(a.seqlens, b, cap, nullptr), kTile);
+  float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC;
+  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC;
+  if (nb == 0) {
+    for (int d = lane; d < kDC; d += 32) {
+      if (ZF32) zf[d] = 0.f; else zb[d] = __float2bfloat16_rn(0.f);
+    }
+    if (lane == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
+    return;
+  }
+  const int g0 = worker_of(Sb, T, G), g1 = worker_of(Sb + nb - 1, T, G);
+  // pass 1: the largest reference maximum
+  float M = -INFINITY;
+  for (int g = g0 + lane; g <= g1; g += 32) {
+    const bool live = worker_begin(g + 1, T, G) > worker_begin(g, T, G);
+    if (live) M = fmaxf(M, m_part[((int64_t)g + b) * kH + h]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // pass 2: weights (one worker per lane, 32 at a time) and the weighted sum
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  for (int c0 = g0; c0 <= g1; c0 += 32) {
+    const int g = c0 + lane;
+    float wgt = 0.f;
+    if (g <= g1 && worker_begin(g + 1, T, G) > worker_begin(g, T, G)) {
+      const int64_t slot = (int64_t)g + b;
+      wgt = exp2f(m_part[slot * kH + h] - M);
+      L += wgt * l_part[slot * kH + h];
+    }
+    const int cnt = min(32, g1 - c0 + 1);
+    for (int i = 0; i < cnt; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, wgt, i);
+      if (wi == 0.f) continue;
+      const float4* src = reinterpret_cast<const float4*>(a.o_part + (((int64_t)c0 + i + b) * kH + h) * kDC);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[lane + 32 * q];
+        acc[q].x += wi * v.x;
+        acc[q].y += wi * v.y;
+        acc[q].z += wi * v.z;
+        acc[q].w += wi * v.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = 1.f / L;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int d = (lane + 32 * q) * 4;
+    const float4 v = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+    if (ZF32) {
+      *reinterpret_cast<float4*>(zf + d) = v;
+    } else {
+      *reinterpret_cast<uint2*>(zb + d) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+  }
+  if (lane == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = (M + log2f(L)) * kLn2;
 }
 
 // ---------------------------------------------------------------- host side
@@ -508,9 +764,9 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   dims[0] = kD;
   strides[0] = (cuuint64_t)kD * 2;
   if (a.block_table) {
-    dims[1] = kTileTokens;
+    dims[1] = 64;
     dims[2] = (cuuint64_t)a.num_blocks;
-    strides[1] = (cuuint64_t)kTileTokens * kD * 2;
+    strides[1] = (cuuint64_t)64 * kD * 2;
   } else {
     dims[1] = (cuuint64_t)a.seq_stride;
     dims[2] = (cuuint64_t)a.batch;
@@ -532,12 +788,18 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   p.scale_log2 = a.scale * kLog2e;
   p.workers = a.workers;
   p.o_part = a.o_part;
-  p.lse_part = a.lse_part;
+  p.m_part = a.lse_part;
+  p.l_part = a.l_part;
   p.status = a.status;
   const size_t smem = tc_smem_bytes(a.batch);
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 grid(kH / 4, a.batch);
+  if (a.z_is_fp32) combine_tc_kernel<true><<<grid, 128, 0, s>>>(a);
+  else combine_tc_kernel<false><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -29,7 +29,8 @@ struct DecodeLaunch {
   float scale;
   int32_t workers;        // G
   float* o_part;          // [(G + B)][n_h][d_c]
-  float* lse_part;        // [(G + B)][n_h]
+  float* lse_part;        // [(G + B)][n_h]  generic: lse; tensor-core: reference maximum (log2)
+  float* l_part;          // [(G + B)][n_h]  tensor-core: weight sum relative to the maximum
   void* z_out;
   int32_t z_is_fp32;
   float* lse_out;
@@ -41,8 +42,8 @@ cudaError_t launch_decode_generic(const DecodeLaunch& a, int num_sms, cudaStream
 cudaError_t launch_combine(const DecodeLaunch& a, cudaStream_t s);
 int generic_head_groups(int n_heads);
 
-// Tensor-core (tcgen05) decode for n_h = 128, d_c = 512, d_R = 64: `workers`
-// is the number of CTA pairs (clusters of two).
+// Tensor-core (tcgen05) decode for n_h = 128, d_c = 512, d_R = 64, partial pass
+// and its combine: `workers` is the number of CTA pairs (clusters of two).
 bool tc_supported(const DecodeLaunch& a);
 cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
 size_t generic_smem_bytes(int D, int batch);

@@ -28,7 +28,7 @@ MLA_DEVI int effective_len(const int32_t* seqlens, int b, int64_t capacity, int3
   return L;
 }
 
-MLA_DEVI int tiles_of(int L) { return (L + kTileTokens - 1) / kTileTokens; }
+MLA_DEVI int tiles_of(int L, int tile = kTileTokens) { return (L + tile - 1) / tile; }
 
 MLA_DEVI int64_t worker_begin(int g, int64_t T, int G) { return (int64_t)g * T / G; }
 
@@ -38,15 +38,16 @@ MLA_DEVI int worker_of(int64_t x, int64_t T, int G) {
   return (int)(g < G - 1 ? g : G - 1);
 }
 
-// Exclusive prefix of tiles_of(effective_len(b)) over b into pre[0..B]
+// Exclusive prefix of tiles_of(effective_len(b), tile) over b into pre[0..B]
 // (shared memory); every thread of the block takes part.  Invalid lengths
 // are reported once, by the thread that scans them.
-MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* status, int* pre) {
+MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* status, int* pre,
+                          int tile = kTileTokens) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int per = (B + nthr - 1) / nthr;
   const int b0 = tid * per, b1 = min(B, b0 + per);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += tiles_of(effective_len(seqlens, b, cap, status));
+  for (int b = b0; b < b1; ++b) local += tiles_of(effective_len(seqlens, b, cap, status), tile);
   __shared__ int warp_sums[32];
   const int lane = tid & 31, warp = tid >> 5;
   int incl = local;
@@ -62,7 +63,7 @@ MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* s
   int run = warp_off + incl - local;
   for (int b = b0; b < b1; ++b) {
     pre[b] = run;
-    run += tiles_of(effective_len(seqlens, b, cap, nullptr));
+    run += tiles_of(effective_len(seqlens, b, cap, nullptr), tile);
   }
   if (tid == nthr - 1) pre[B] = run;  // the last thread's running sum is the total
   __syncthreads();
