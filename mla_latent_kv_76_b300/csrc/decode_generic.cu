@@ -318,8 +318,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeLaunch a) {
 template <int DC>
 static cudaError_t launch_generic_dc(const DecodeLaunch& a, cudaStream_t s) {
   const GenericSmem L = generic_smem(DC + a.d_rope, a.batch);
-  cudaError_t e = cudaFuncSetAttribute(decode_generic_kernel<DC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  cudaError_t e = ensure_smem<decode_generic_kernel<DC>>(L.total);
   if (e != cudaSuccess) return e;
   dim3 grid(a.workers, generic_head_groups(a.n_heads));
   decode_generic_kernel<DC><<<grid, 128, L.total, s>>>(a);

@@ -19,13 +19,15 @@
 // Every cache byte is read from HBM once by the score CTA; the value CTA
 // re-reads the latent columns a few microseconds later, from L2.
 //
-// Score CTA, 384 threads: warp 0 TMA (12 ring slots of 128 tokens x 64
-// columns, 128-byte swizzle), warp 1 MMA issue, warps 4-7 / 8-11 softmax for
-// token columns 0-63 / 64-127 (thread = head).
+// Score CTA, 384 threads: warp 0 TMA (10 ring slots of 128 tokens x 64
+// columns, 128-byte swizzle), warp 1 MMA issue (S double-buffered in TMEM),
+// warps 4-7 / 8-11 softmax for token columns 0-63 / 64-127 (thread = head),
+// warps 2 / 3 ship each warpgroup's P to the value CTA as one bulk copy.
 // Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns), warp 1 MMA,
 // warps 2-3 zero the rows past the sequence end in the last half tile (NaN
 // garbage must not meet a zero weight), warps 4-7 rescale O and write the
-// segment's partial (thread = head), warp 8 returns P buffers to the score CTA.
+// segment's partial (thread = head), warp 8 returns P buffers to the score CTA
+// once O has consumed them, warp 9 frees the score CTA's staging once P landed.
 //
 // Online softmax with a lazily updated reference maximum m_ref (base 2):
 // P = 2^(x - m_ref); m_ref moves, and O and l are rescaled, only when a tile's
@@ -48,39 +50,46 @@ constexpr int kTile = 128;           // tokens per score tile (two 64-token halv
 constexpr int kThreads = 384;
 constexpr int kTcMaxBatch = 1024;
 constexpr float kRescaleThreshold = 16.f;
+constexpr int kPrefetchTiles = 4;    // the score CTA's producer warms L2 this many tiles ahead
 
+// ---- P hand-off unit: 64 tokens of bf16 weights for 128 heads, then metadata
+constexpr int kPBytes = kH * 128;                  // 128 heads x 64 tokens bf16 (SW128 K-major)
+constexpr int kPMetaAlpha = kPBytes;               // alpha[128] fp32
+constexpr int kPMetaFlags = kPBytes + 512;         // flag[4] int32 (per warp: O must be rescaled)
+constexpr int kPBufBytes = kPBytes + 1024;
 // ---- score CTA shared memory
-constexpr int kSlots = 12;
+constexpr int kSlots = 10;
 constexpr int kSlotBytes = kTile * 128;            // 128 tokens x 64 bf16 columns
 constexpr int kOffRing = 0;
-constexpr int kOffXmax = kOffRing + kSlots * kSlotBytes;   // [2 parity][2 wg][128] fp32
+constexpr int kOffQrope = kOffRing + kSlots * kSlotBytes;  // RoPE part of Q, 128 heads x 64 bf16 (SW128)
+constexpr int kOffStaging = kOffQrope + kH * 128;          // [2 wg] P hand-off staging
+constexpr int kOffXmax = kOffStaging + 2 * kPBufBytes;     // [2 parity][2 wg][128] fp32
 constexpr int kOffLsum = kOffXmax + 2 * 2 * kH * 4;        // [128] fp32
 // ---- value CTA shared memory
 constexpr int kVStages = 2;
 constexpr int kChunkBytes = 64 * 128;              // 64 tokens x 64 bf16 columns
 constexpr int kVStageBytes = 8 * kChunkBytes;      // the 512 latent columns of 64 tokens
 constexpr int kPBufs = 4;
-constexpr int kPBytes = kH * 128;                  // 128 heads x 64 tokens bf16
-constexpr int kMetaBytes = 1024;                   // alpha[128] fp32, flag[4] int32
 constexpr int kOffStage = 0;
-constexpr int kOffP = kOffStage + kVStages * kVStageBytes;
-constexpr int kOffMeta = kOffP + kPBufs * kPBytes;
+constexpr int kOffP = kOffStage + kVStages * kVStageBytes;  // [4] P hand-off buffers
 // ---- common tail
-constexpr int kOffBar = (kOffLsum + kH * 4 > kOffMeta + kPBufs * kMetaBytes) ? kOffLsum + kH * 4
-                                                                             : kOffMeta + kPBufs * kMetaBytes;
+constexpr int kOffBar = (kOffLsum + kH * 4 > kOffP + kPBufs * kPBufBytes) ? kOffLsum + kH * 4
+                                                                         : kOffP + kPBufs * kPBufBytes;
 constexpr int kNumBars = 40;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, event descriptor
 constexpr int kOffPrefix = kOffMisc + 32;
 
 // score CTA barriers
-constexpr int kBarCfull = 0, kBarCempty = 12, kBarSfull = 24, kBarSfree = 25, kBarQready = 26, kBarPfree = 27,
-              kBarScDrained = 31, kBarXmax = 32, kBarLsum = 34;
+constexpr int kBarCfull = 0, kBarCempty = 10, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
+              kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35;
 // value CTA barriers
 constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOdone = 10, kBarOcomp = 14, kBarEvt = 15,
               kBarEvtdone = 16, kBarVcDrained = 17;
 
 // TMEM columns
-constexpr uint32_t kColS = 0, kColQ = 128;  // score CTA (S: 128 tokens, Q: 576 bf16 packed in 288 columns)
+// score CTA: S double buffer [0, 256) (128 tokens each), the query's 512 latent
+// columns as packed bf16 [256, 512); its 64 RoPE columns live in shared memory
+constexpr uint32_t kColS = 0, kColQ = 256;
 
 enum { kEvtRescale = 1, kEvtEpilogue = 2, kEvtExit = 3 };
 
@@ -88,6 +97,7 @@ size_t tc_smem_bytes(int batch) { return (size_t)kOffPrefix + (size_t)(batch + 1
 
 struct TcParams {
   const __nv_bfloat16* q;
+  const __nv_bfloat16* pool;
   const int32_t* block_table;
   int32_t max_blocks;
   int32_t num_blocks;
@@ -97,7 +107,7 @@ struct TcParams {
   int32_t paged;
   float scale_log2;
   int32_t workers;  // CTA pairs
-  float* o_part;    // [(G + B)][128][512]  unnormalised
+  float* o_part;    // [(G + B)][128 float4 columns][128 heads][4]  unnormalised
   float* m_part;    // [(G + B)][128]       reference maximum, log2 units
   float* l_part;    // [(G + B)][128]       sum of weights relative to m_part
   int32_t* status;
@@ -155,8 +165,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[kBarCfull + i], 1);
         tc::mbar_init(&bars[kBarCempty + i], 1);
       }
-      tc::mbar_init(&bars[kBarSfull], 1);
-      tc::mbar_init(&bars[kBarSfree], 256);
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&bars[kBarSfull + i], 1);
+        tc::mbar_init(&bars[kBarSfree + i], 256);
+        tc::mbar_init(&bars[kBarStgFull + i], 128);
+        tc::mbar_init(&bars[kBarStgFree + i], 1);
+      }
       tc::mbar_init(&bars[kBarQready], 256);
       for (int i = 0; i < kPBufs; ++i) tc::mbar_init(&bars[kBarPfree + i], 1);
       tc::mbar_init(&bars[kBarScDrained], 1);
@@ -170,7 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[kBarFix + i], 64);
       }
       for (int i = 0; i < kPBufs; ++i) {
-        tc::mbar_init(&bars[kBarPfull + i], 128);
+        tc::mbar_init(&bars[kBarPfull + i], 1);  // the score CTA's expect_tx arrival + the copy
         tc::mbar_init(&bars[kBarOdone + i], 1);
       }
       tc::mbar_init(&bars[kBarOcomp], 1);
@@ -201,10 +215,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::prefetch_map(&cache_map);
         int n = 0;  // chunk counter: 9 per tile
         bool ok = true;
+        // The ring holds ~1 tile, less than HBM latency covers at full rate: tiles
+        // kPrefetchTiles ahead are pulled into L2 first, so the ring loads hit L2.
+        auto prefetch_tile = [&](int64_t xt) {
+          const int b = seq_of_tile(pre, B, xt);
+          const int tt = (int)(xt - pre[b]);
+          const int L = effective_len(p.seqlens, b, cap, nullptr);
+          const int nh = min(2, (L - tt * kTile + 63) >> 6);
+          for (int w = 0; w < nh; ++w) {
+            const int rows = min(64, L - tt * kTile - 64 * w);
+            const __nv_bfloat16* src;
+            if (p.paged) {
+              const int lb = 2 * tt + w;
+              if (lb >= p.max_blocks) continue;
+              const int blk = p.block_table[(int64_t)b * p.max_blocks + lb];
+              if (blk < 0 || blk >= p.num_blocks) continue;
+              src = p.pool + (int64_t)blk * 64 * kD;
+            } else {
+              src = p.pool + ((int64_t)b * p.seq_stride + tt * kTile + 64 * w) * kD;
+            }
+            tc::prefetch_l2(src, (uint32_t)rows * kD * 2);
+          }
+        };
+        for (int64_t xt = lo; xt < hi && xt < lo + kPrefetchTiles; ++xt) prefetch_tile(xt);
+        int64_t xg = lo;  // global index of the tile being loaded
         for (int64_t x = lo; x < hi && ok;) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
           x += s.ntile;
-          for (int j = 0; j < s.ntile && ok; ++j) {
+          for (int j = 0; j < s.ntile && ok; ++j, ++xg) {
+            if (xg + kPrefetchTiles < hi) prefetch_tile(xg + kPrefetchTiles);
             const int tt = s.t_begin + j;
             const int nh = halves_of(s, tt);
             int blk[2] = {-1, -1};
@@ -258,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- score MMA
         constexpr uint32_t idS = tc::idesc_bf16(128, kTile, 0, 0);
         const uint32_t ring = smem_u32(sm + kOffRing);
+        const uint32_t qrope = smem_u32(sm + kOffQrope);
         int n = 0, m = 0, k = 0;
         bool ok = true;
         for (int64_t x = lo; x < hi && ok; ++k) {
@@ -265,30 +305,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           x += s.ntile;
           if (!tc::wait<false>(&bars[kBarQready], k & 1, ab)) break;
           for (int j = 0; j < s.ntile && ok; ++j, ++m) {
-            if (m >= 1 && !tc::wait<false>(&bars[kBarSfree], (m - 1) & 1, ab)) {
+            // S is double-buffered: buffer m & 1 is free once the softmax read tile m - 2
+            if (m >= 2 && !tc::wait<false>(&bars[kBarSfree + (m & 1)], ((m >> 1) - 1) & 1, ab)) {
               ok = false;
               break;
             }
             tc::tc_fence_after();
-            for (int c = 0; c < 9; ++c, ++n) {
-              const int sl = n % kSlots;
-              if (!tc::wait<false>(&bars[kBarCfull + sl], (n / kSlots) & 1, ab)) {
+            const uint32_t dS = tb + kColS + (m & 1) * kTile;
+            // straight-line issue: per 64-column chunk one wait, four MMAs, one commit
+#pragma unroll
+            for (int c = 0; c < 9; ++c) {
+              const int sl = (n + c) % kSlots;
+              if (!tc::wait<false>(&bars[kBarCfull + sl], ((n + c) / kSlots) & 1, ab)) {
                 ok = false;
                 break;
               }
               tc::tc_fence_after();
               const uint32_t sa = ring + sl * kSlotBytes;
+              if (c < 8) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc::mma_ts(tb + kColS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
-                           (c | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk)
+                  tc::mma_ts(dS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
+                             (c | kk) != 0 ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc::mma_ss(dS, tc::smem_desc(qrope + kk * 32, 16, 1024), tc::smem_desc(sa + kk * 32, 16, 1024), idS,
+                             1u);
+              }
               tc::mma_commit(&bars[kBarCempty + sl]);
             }
-            if (ok) tc::mma_commit(&bars[kBarSfull]);
+            n += 9;
+            if (ok) tc::mma_commit(&bars[kBarSfull + (m & 1)]);
           }
         }
         tc::mma_commit(&bars[kBarScDrained]);
         tc::wait<false>(&bars[kBarScDrained], 0, ab);
+      }
+    } else if (warp == 2 || warp == 3) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- P hand-off for warpgroup (warp - 2)
+        const int w = warp - 2;
+        uint8_t* stg = sm + kOffStaging + w * kPBufBytes;
+        const uint32_t r_p = tc::map_peer(sm + kOffP, 1);
+        const uint32_t r_pfull = tc::map_peer(&bars[kBarPfull], 1);
+        int hh = 0, u = 0;
+        bool ok = true;
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j) {
+            const int nh = halves_of(s, s.t_begin + j);
+            if (w < nh) {
+              const int hidx = hh + w;
+              const int pb = hidx % kPBufs, up = hidx / kPBufs;
+              if (!tc::wait<false>(&bars[kBarStgFull + w], u & 1, ab)) { ok = false; break; }
+              if (up >= 1 && !tc::wait<true>(&bars[kBarPfree + pb], (up - 1) & 1, ab)) { ok = false; break; }
+              // the value CTA's warp 9 frees the staging (kBarStgFree) once the copy landed
+              tc::bulk_copy_to_peer(r_p + pb * kPBufBytes, stg, kPBufBytes, r_pfull + pb * 8);
+              ++u;
+            }
+            hh += nh;
+          }
+        }
       }
     } else if (warp >= 4) {
       // ------------------------------------------------------------ softmax (thread = head)
@@ -297,13 +376,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
       float* xmax = reinterpret_cast<float*>(sm + kOffXmax);
       float* lsum = reinterpret_cast<float*>(sm + kOffLsum);
-      // the value CTA's P buffers, metadata and arrival barriers
-      const uint32_t r_p = tc::map_peer(sm + kOffP, 1);
-      const uint32_t r_meta = tc::map_peer(sm + kOffMeta, 1);
-      const uint32_t r_pfull = tc::map_peer(&bars[kBarPfull], 1);
+      uint8_t* stg = sm + kOffStaging + w * kPBufBytes;  // this warpgroup's P hand-off staging
+      int sends = 0;
 
       auto load_q = [&](int b) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * kH + h) * kD + 288 * w);
+        const __nv_bfloat16* row = p.q + ((int64_t)b * kH + h) * kD;
+        const uint4* src = reinterpret_cast<const uint4*>(row + 256 * w);  // latent [256 w, 256 w + 256)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -315,18 +393,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             r[4 * i + 2] = v.z;
             r[4 * i + 3] = v.w;
           }
-          tc::tmem_st32(lane_t + kColQ + 144 * w + c * 32, r);
+          tc::tmem_st32(lane_t + kColQ + 128 * w + c * 32, r);
         }
-        uint32_t r[16];
+        // RoPE columns [32 w, 32 w + 32) of the row: 16-byte pieces 4 w .. 4 w + 3 of a
+        // 128-byte-swizzled K-major row
+        const uint4* srcr = reinterpret_cast<const uint4*>(row + kDC);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 v = __ldg(src + 32 + i);
-          r[4 * i] = v.x;
-          r[4 * i + 1] = v.y;
-          r[4 * i + 2] = v.z;
-          r[4 * i + 3] = v.w;
-        }
-        tc::tmem_st16(lane_t + kColQ + 144 * w + 128, r);
+        for (int c = 4 * w; c < 4 * w + 4; ++c)
+          *reinterpret_cast<uint4*>(sm + kOffQrope + h * 128 + ((c ^ (h & 7)) * 16)) = __ldg(srcr + c);
+        tc::fence_async_smem();
         tc::tmem_wait_st();
         tc::tc_fence_before();
         tc::mbar_arrive(&bars[kBarQready]);
@@ -343,26 +418,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = 0; j < s.ntile; ++j, ++m) {
           const int tt = s.t_begin + j;
           const int nh = halves_of(s, tt);
-          if (!tc::wait<false>(&bars[kBarSfull], m & 1, ab)) {
+          if (!tc::wait<false>(&bars[kBarSfull + (m & 1)], (m >> 1) & 1, ab)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
           uint32_t sa[32], sb[32];
-          tc::tmem_ld32(lane_t + kColS + 64 * w, sa);
-          tc::tmem_ld32(lane_t + kColS + 64 * w + 32, sb);
+          const uint32_t sc = lane_t + kColS + (m & 1) * kTile + 64 * w;
+          tc::tmem_ld32(sc, sa);
+          tc::tmem_ld32(sc + 32, sb);
           tc::tmem_wait_ld();
           tc::tc_fence_before();
-          tc::mbar_arrive(&bars[kBarSfree]);
+          tc::mbar_arrive(&bars[kBarSfree + (m & 1)]);
           const int nvalid = s.len - tt * kTile - 64 * w;  // may be <= 0
           float xv[64];
-          float mt = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const float sv = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
             xv[c] = (c < nvalid) ? sv * p.scale_log2 : -INFINITY;
-            mt = fmaxf(mt, xv[c]);
           }
+          float mx[8];  // tree maximum (independent chains)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(xv[i], xv[i + 8]), fmaxf(xv[i + 16], xv[i + 24]));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], fmaxf(fmaxf(xv[i + 32], xv[i + 40]), fmaxf(xv[i + 48], xv[i + 56])));
+          float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
           // tile maximum over both halves (bounded rendezvous of the two warpgroups)
           float* xm = xmax + (m & 1) * 2 * kH;
           xm[w * kH + h] = mt;
@@ -382,27 +462,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           // P = 2^(x - m_ref) in bf16; l sums the rounded weights
           uint32_t pk[32];
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            pk[i] = pack_bf16x2(exp2f(xv[2 * i] - m_ref), exp2f(xv[2 * i + 1] - m_ref));
-            l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            pk[i] = pack_bf16x2(tc::ex2(xv[2 * i] - m_ref), tc::ex2(xv[2 * i + 1] - m_ref));
+            ls[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
           }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
           if (w < nh) {
-            const int hidx = hh + w;
-            const int pb = hidx % kPBufs, u = hidx / kPBufs;
-            if (u >= 1 && !tc::wait<true>(&bars[kBarPfree + pb], (u - 1) & 1, ab)) {
+            // stage this half's P (+ alpha and per-warp rescale flags); warp 2 + w ships it
+            if (sends >= 1 && !tc::wait<false>(&bars[kBarStgFree + w], (sends - 1) & 1, ab)) {
               ok = false;
               break;
             }
-            const uint32_t row = r_p + pb * kPBytes + h * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              tc::st_cluster_u4(row + ((c ^ (h & 7)) * 16), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            const uint32_t meta = r_meta + pb * kMetaBytes;
+              *reinterpret_cast<uint4*>(stg + h * 128 + ((c ^ (h & 7)) * 16)) =
+                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             const bool any = __any_sync(0xffffffffu, alpha != 1.f);
-            if (w == 0) tc::st_cluster_u32(meta + h * 4, __float_as_uint(alpha));
-            if (lane == 0) tc::st_cluster_u32(meta + 512 + (warp & 3) * 4, (w == 0 && any) ? 1u : 0u);
-            tc::mbar_arrive_cluster_addr(r_pfull + pb * 8);
+            if (w == 0) reinterpret_cast<float*>(stg + kPMetaAlpha)[h] = alpha;
+            if (lane == 0) reinterpret_cast<int*>(stg + kPMetaFlags)[warp & 3] = (w == 0 && any) ? 1 : 0;
+            tc::fence_async_smem();
+            tc::mbar_arrive(&bars[kBarStgFull + w]);
+            ++sends;
           }
           hh += nh;
         }
@@ -472,7 +554,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         constexpr uint32_t idO = tc::idesc_bf16(128, 256, 0, 1);
         const uint32_t stg0 = smem_u32(sm + kOffStage);
         const uint32_t pb0 = smem_u32(sm + kOffP);
-        const volatile int* meta_flags = reinterpret_cast<const volatile int*>(sm + kOffMeta + 512);
         int hh = 0, oc = 0, ev = 0;
         int ntail[kVStages] = {0, 0};
         bool ok = true;
@@ -502,13 +583,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!tc::wait<false>(&bars[kBarFix + st], ntail[st] & 1, ab)) { ok = false; break; }
                 ++ntail[st];
               }
-              if (!tc::wait<true>(&bars[kBarPfull + pb], (hh / kPBufs) & 1, ab)) { ok = false; break; }
-              const volatile int* fl = meta_flags + pb * (kMetaBytes / 4);
+              if (!tc::wait<false>(&bars[kBarPfull + pb], (hh / kPBufs) & 1, ab)) { ok = false; break; }
+              const volatile int* fl = reinterpret_cast<const volatile int*>(sm + kOffP + pb * kPBufBytes + kPMetaFlags);
               if (fl[0] | fl[1] | fl[2] | fl[3]) {  // the reference maximum moved: rescale O first
                 if (!drain() || !post(kEvtRescale, pb, 0)) { ok = false; break; }
               }
               tc::tc_fence_after();
-              const uint32_t sa = stg0 + st * kVStageBytes, pa = pb0 + pb * kPBytes;
+              const uint32_t sa = stg0 + st * kVStageBytes, pa = pb0 + pb * kPBufBytes;
 #pragma unroll
               for (int n2 = 0; n2 < 2; ++n2)
 #pragma unroll
@@ -572,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int type = evt_desc[0], arg = evt_desc[1], slot = evt_desc[2];
         if (type == kEvtExit) break;
         if (type == kEvtRescale) {
-          const float a = reinterpret_cast<const float*>(sm + kOffMeta + arg * kMetaBytes)[h];
+          const float a = reinterpret_cast<const float*>(sm + kOffP + arg * kPBufBytes + kPMetaAlpha)[h];
 #pragma unroll 1
           for (int c = 0; c < 16; ++c) {
             uint32_t r[32];
@@ -584,21 +665,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc::tmem_wait_st();
         } else {
-          float* dst = p.o_part + ((int64_t)slot * kH + h) * kDC;
+          // partial layout [slot][128 float4 columns j][128 heads][4]: for each j the
+          // 32 lanes of a warp store 512 contiguous bytes
+          float4* dst = reinterpret_cast<float4*>(p.o_part) + (int64_t)slot * (kDC / 4) * kH + h;
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            uint32_t r[32];
-            tc::tmem_ld32(lane_t + c * 32, r);
+          for (int c = 0; c < 16; c += 2) {
+            uint32_t r0[32], r1[32];
+            tc::tmem_ld32(lane_t + c * 32, r0);
+            tc::tmem_ld32(lane_t + c * 32 + 32, r1);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              reinterpret_cast<float4*>(dst + c * 32)[i] =
-                  make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
-                              __uint_as_float(r[4 * i + 3]));
+            for (int i = 0; i < 8; ++i) {
+              dst[(c * 8 + i) * kH] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
+                                                  __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
+              dst[(c * 8 + 8 + i) * kH] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
+                                                      __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
+            }
           }
         }
         tc::tc_fence_before();
         tc::mbar_arrive(&bars[kBarEvtdone]);
+      }
+    } else if (warp == 9) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- P landed: the score CTA may reuse its staging
+        const uint32_t r_stgfree = tc::map_peer(&bars[kBarStgFree], 0);
+        int hh = 0;
+        bool ok = true;
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j) {
+            const int nh = halves_of(s, s.t_begin + j);
+            for (int w = 0; w < nh; ++w, ++hh) {
+              if (!tc::wait<false>(&bars[kBarPfull + hh % kPBufs], (hh / kPBufs) & 1, ab)) {
+                ok = false;
+                break;
+              }
+              tc::mbar_arrive_cluster_addr(r_stgfree + w * 8);
+            }
+          }
+        }
       }
     } else if (warp == 8) {
       if (lane == 0) {
@@ -638,17 +745,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ combine
 // Partials are unnormalised: O_s with reference maximum m_s (log2 units) and
 // weight sum l_s.  M = max_s m_s, L = sum_s l_s 2^(m_s - M),
-// z = sum_s 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.  One warp per head.
+// z = sum_s 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.
+// Block (column group of 32, sequence b), thread = head: the partial reads are
+// 512 contiguous bytes per warp.
 template <bool ZF32>
 __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
-  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 4 + warp;
+  const int jg = blockIdx.x, b = blockIdx.y, h = threadIdx.x, warp = h >> 5, lane = h & 31;
   const int G = a.workers;
   const float* m_part = a.lse_part;
   const float* l_part = a.l_part;
   const int64_t cap = a.block_table ? (int64_t)a.max_blocks * 64 : a.seq_stride;
   long long before = 0, total = 0;
-  for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+  for (int i = h; i < a.batch; i += blockDim.x) {
     const int t = tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile);
     total += t;
     if (i < b) before += t;
@@ -666,68 +774,50 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
   __syncthreads();
   const int64_t Sb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   const int64_t T = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  if (h >= kH) return;
   const int nb = tiles_of(effective_len(a.seqlens, b, cap, nullptr), kTile);
-  float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC;
-  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC;
+  float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 32;
+  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 32;
   if (nb == 0) {
-    for (int d = lane; d < kDC; d += 32) {
+    for (int d = 0; d < 32; ++d) {
       if (ZF32) zf[d] = 0.f; else zb[d] = __float2bfloat16_rn(0.f);
     }
-    if (lane == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
+    if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
     return;
   }
   const int g0 = worker_of(Sb, T, G), g1 = worker_of(Sb + nb - 1, T, G);
-  // pass 1: the largest reference maximum
   float M = -INFINITY;
-  for (int g = g0 + lane; g <= g1; g += 32) {
-    const bool live = worker_begin(g + 1, T, G) > worker_begin(g, T, G);
-    if (live) M = fmaxf(M, m_part[((int64_t)g + b) * kH + h]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  // pass 2: weights (one worker per lane, 32 at a time) and the weighted sum
-  float4 acc[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g = g0; g <= g1; ++g)
+    if (worker_begin(g + 1, T, G) > worker_begin(g, T, G)) M = fmaxf(M, m_part[((int64_t)g + b) * kH + h]);
   float L = 0.f;
-  for (int c0 = g0; c0 <= g1; c0 += 32) {
-    const int g = c0 + lane;
-    float wgt = 0.f;
-    if (g <= g1 && worker_begin(g + 1, T, G) > worker_begin(g, T, G)) {
-      const int64_t slot = (int64_t)g + b;
-      wgt = exp2f(m_part[slot * kH + h] - M);
-      L += wgt * l_part[slot * kH + h];
-    }
-    const int cnt = min(32, g1 - c0 + 1);
-    for (int i = 0; i < cnt; ++i) {
-      const float wi = __shfl_sync(0xffffffffu, wgt, i);
-      if (wi == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(a.o_part + (((int64_t)c0 + i + b) * kH + h) * kDC);
+  float4 acc[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[lane + 32 * q];
-        acc[q].x += wi * v.x;
-        acc[q].y += wi * v.y;
-        acc[q].z += wi * v.z;
-        acc[q].w += wi * v.w;
-      }
+  for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g = g0; g <= g1; ++g) {
+    if (worker_begin(g + 1, T, G) <= worker_begin(g, T, G)) continue;  // idle worker: no partial
+    const int64_t slot = (int64_t)g + b;
+    const float wgt = exp2f(m_part[slot * kH + h] - M);
+    L += wgt * l_part[slot * kH + h];
+    const float4* src = reinterpret_cast<const float4*>(a.o_part) + (slot * (kDC / 4) + jg * 8) * kH + h;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = src[i * kH];
+      acc[i].x += wgt * v.x;
+      acc[i].y += wgt * v.y;
+      acc[i].z += wgt * v.z;
+      acc[i].w += wgt * v.w;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = 1.f / L;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int d = (lane + 32 * q) * 4;
-    const float4 v = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
     if (ZF32) {
-      *reinterpret_cast<float4*>(zf + d) = v;
+      reinterpret_cast<float4*>(zf)[i] = v;
     } else {
-      *reinterpret_cast<uint2*>(zb + d) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      reinterpret_cast<uint2*>(zb)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
     }
   }
-  if (lane == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = (M + log2f(L)) * kLn2;
+  if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = (M + log2f(L)) * kLn2;
 }
 
 // ---------------------------------------------------------------- host side
@@ -778,6 +868,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   TcParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.pool = static_cast<const __nv_bfloat16*>(a.pool);
   p.block_table = a.block_table;
   p.max_blocks = a.max_blocks;
   p.num_blocks = a.num_blocks;
@@ -792,12 +883,12 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   p.l_part = a.l_part;
   p.status = a.status;
   const size_t smem = tc_smem_bytes(a.batch);
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem<decode_tc_kernel>((int)smem);
   if (e != cudaSuccess) return e;
   decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid(kH / 4, a.batch);
+  dim3 grid(kDC / 32, a.batch);
   if (a.z_is_fp32) combine_tc_kernel<true><<<grid, 128, 0, s>>>(a);
   else combine_tc_kernel<false><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();

@@ -213,9 +213,22 @@ __global__ void __launch_bounds__(128) sgemm_kernel(const GemmArgs a) {
   }
 
   // ------------------------------------------------------------ epilogue
-  if (EP == Epi::APPEND || EP == Epi::ABSORB) {
-    for (int i = tid; i < a.d_rope / 2 && i < 64; i += 128)
-      s_theta[i] = pow((double)a.rope_base, -2.0 * (double)i / (double)a.d_rope);
+  // RoPE frequencies theta_i = base^(-2i/d_R) in fp64, only in CTAs that rotate
+  // something: one pow for r = base^(-2/d_R), then theta_i = r^i by squaring
+  // (FP64 throughput is low on this part; 32 pows per CTA would dominate).
+  const bool needs_theta = (EP == Epi::APPEND && n0 + BN > a.d_latent) || (EP == Epi::ABSORB && blockIdx.x == 0);
+  if (needs_theta) {
+    __shared__ double s_r;
+    if (tid == 0) s_r = pow((double)a.rope_base, -2.0 / (double)a.d_rope);
+    __syncthreads();
+    for (int i = tid; i < a.d_rope / 2 && i < 64; i += 128) {
+      double t = 1.0, base = s_r;
+      for (int e = i; e; e >>= 1) {
+        if (e & 1) t *= base;
+        base *= base;
+      }
+      s_theta[i] = t;
+    }
     __syncthreads();
   }
   for (int i = tid; i < BM * (BN / 2); i += 128) {
@@ -281,7 +294,7 @@ template <int BM, int BN, int BK, int STAGES, WLayout WL, Epi EP>
 static cudaError_t run(GemmArgs a, int groups, int ksplit, cudaStream_t s) {
   using C = GemmCfg<BM, BN, BK, STAGES, WL>;
   auto kern = sgemm_kernel<BM, BN, BK, STAGES, WL, EP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_smem<sgemm_kernel<BM, BN, BK, STAGES, WL, EP>>(C::SMEM);
   if (e != cudaSuccess) return e;
   a.ksplit = ksplit;
   const int ntiles = (a.N + BN - 1) / BN;
@@ -379,18 +392,21 @@ cudaError_t launch_append(const mla_dims& d, int n_tokens, int d_model, const vo
   a.block_tokens = d.block_tokens;
   a.seq_stride = seq_stride;
   a.status = status;
-  // split K over a cluster so that about one CTA per SM streams the weights
+  // split K over a cluster so that about one CTA per SM streams the weights,
+  // with (for 16 tokens) the CTA's whole K slice in flight at once; every
+  // cluster of the launch must be co-resident (about 15 clusters of 8 fit at
+  // one ~126 KB CTA per SM, so larger tiles use clusters of at most 4)
   const int ntiles = (D + 31) / 32;
-  auto split = [&](int bm, int bk) {
+  auto split = [&](int bm, int bk, int kmax_cluster) {
     const int mt = (n_tokens + bm - 1) / bm;
     int ks = (148 + ntiles * mt - 1) / (ntiles * mt);
     const int kmax = (d_model + bk - 1) / bk;
-    ks = ks < 1 ? 1 : (ks > 8 ? 8 : ks);
+    ks = ks < 1 ? 1 : (ks > kmax_cluster ? kmax_cluster : ks);
     return ks > kmax ? kmax : ks;
   };
-  if (n_tokens <= 16) return run<16, 32, 256, 5, WLayout::NK, Epi::APPEND>(a, 1, split(16, 256), s);
-  if (n_tokens <= 32) return run<32, 32, 256, 4, WLayout::NK, Epi::APPEND>(a, 1, split(32, 256), s);
-  return run<64, 32, 128, 5, WLayout::NK, Epi::APPEND>(a, 1, split(64, 128), s);
+  if (n_tokens <= 16) return run<16, 32, 128, 7, WLayout::NK, Epi::APPEND>(a, 1, split(16, 128, 8), s);
+  if (n_tokens <= 32) return run<32, 32, 256, 4, WLayout::NK, Epi::APPEND>(a, 1, split(32, 256, 4), s);
+  return run<64, 32, 128, 5, WLayout::NK, Epi::APPEND>(a, 1, split(64, 128, 4), s);
 }
 
 }  // namespace mla

@@ -4,9 +4,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mla.h"
 
 namespace mla {
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  Done once per (kernel, device) and size increase, so that
+// steady-state launches make no host API call besides the launch itself.
+template <auto Kernel>
+cudaError_t ensure_smem(int bytes) {
+  static std::atomic<int> set_bytes[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev >= 0 && dev < 64 && bytes <= set_bytes[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) set_bytes[dev].store(bytes, std::memory_order_relaxed);
+  return e;
+}
 
 // Tokens per split-KV tile; equal to the paged block size so a tile never
 // straddles two blocks.

@@ -91,6 +91,16 @@ MLA_DEVI void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int
 MLA_DEVI void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
+// Warm L2 with `bytes` (a multiple of 16) of global memory starting at `src`.
+MLA_DEVI void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// 2^x on the special-function unit (flushes denormal results to zero).
+MLA_DEVI float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // Generic-proxy writes to shared memory made visible to the async proxy
 // (TMA / tensor core) before they are read there.
 MLA_DEVI void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -215,6 +225,19 @@ MLA_DEVI void st_cluster_u32(uint32_t addr, uint32_t a) {
 // Arrive on a barrier of another CTA given its shared::cluster address.
 MLA_DEVI void mbar_arrive_cluster_addr(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Copy `bytes` (a multiple of 16) from this CTA's shared memory to another
+// CTA of the cluster (shared::cluster address `dst`) with the bulk-copy
+// engine.  Arrives on the destination's barrier with the byte count as
+// expected transactions; the copy completes that count, so the destination
+// sees the data once the barrier phase completes.  (The source buffer may be
+// reused only after the destination has reported completion.)
+MLA_DEVI void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t dst_bar) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(dst_bar), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(dst_bar)
+               : "memory");
 }
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
 MLA_DEVI void named_sync(int id, int nthreads) {
