@@ -19,8 +19,9 @@
 // Every cache byte is read from HBM once by the score CTA; the value CTA
 // re-reads the latent columns a few microseconds later, from L2.
 //
-// Score CTA, 384 threads: warp 0 TMA (10 ring slots of 128 tokens x 64
-// columns, 128-byte swizzle), warp 1 MMA issue (S double-buffered in TMEM),
+// Score CTA, 384 threads: warp 0 TMA (3 ring slots, each three 64-column
+// chunks of 128 tokens, 128-byte swizzle), warp 1 MMA issue (S double-buffered
+// in TMEM; one barrier wait and one commit per 12 MMAs),
 // warps 4-7 / 8-11 softmax for token columns 0-63 / 64-127 (thread = head),
 // warps 2 / 3 ship each warpgroup's P to the value CTA as one bulk copy.
 // Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns), warp 1 MMA,
@@ -58,8 +59,9 @@ constexpr int kPMetaAlpha = kPBytes;               // alpha[128] fp32
 constexpr int kPMetaFlags = kPBytes + 512;         // flag[4] int32 (per warp: O must be rescaled)
 constexpr int kPBufBytes = kPBytes + 1024;
 // ---- score CTA shared memory
-constexpr int kSlots = 10;
-constexpr int kSlotBytes = kTile * 128;            // 128 tokens x 64 bf16 columns
+constexpr int kChunk128 = kTile * 128;            // 128 tokens x 64 bf16 columns
+constexpr int kSlots = 3;                          // slot t holds chunks 3t .. 3t + 2 of a tile
+constexpr int kSlotBytes = 3 * kChunk128;
 constexpr int kOffRing = 0;
 constexpr int kOffQrope = kOffRing + kSlots * kSlotBytes;  // RoPE part of Q, 128 heads x 64 bf16 (SW128)
 constexpr int kOffStaging = kOffQrope + kH * 128;          // [2 wg] P hand-off staging
@@ -80,7 +82,7 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, eve
 constexpr int kOffPrefix = kOffMisc + 32;
 
 // score CTA barriers
-constexpr int kBarCfull = 0, kBarCempty = 10, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
+constexpr int kBarCfull = 0, kBarCempty = 3, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
               kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35;
 // value CTA barriers
 constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOdone = 10, kBarOcomp = 14, kBarEvt = 15,
@@ -213,7 +215,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // ---------------------------------------------------------- TMA producer
         tc::prefetch_map(&cache_map);
-        int n = 0;  // chunk counter: 9 per tile
         bool ok = true;
         // The ring holds ~1 tile, less than HBM latency covers at full rate: tiles
         // kPrefetchTiles ahead are pulled into L2 first, so the ring loads hit L2.
@@ -237,13 +238,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc::prefetch_l2(src, (uint32_t)rows * kD * 2);
           }
         };
-        for (int64_t xt = lo; xt < hi && xt < lo + kPrefetchTiles; ++xt) prefetch_tile(xt);
-        int64_t xg = lo;  // global index of the tile being loaded
+        int64_t xg = lo;           // global index of the tile being loaded
+        int64_t pf_next = lo + 1;  // next tile to warm in L2
+        int m = 0;                 // tiles loaded so far
         for (int64_t x = lo; x < hi && ok;) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
           x += s.ntile;
-          for (int j = 0; j < s.ntile && ok; ++j, ++xg) {
-            if (xg + kPrefetchTiles < hi) prefetch_tile(xg + kPrefetchTiles);
+          for (int j = 0; j < s.ntile && ok; ++j, ++xg, ++m) {
             const int tt = s.t_begin + j;
             const int nh = halves_of(s, tt);
             int blk[2] = {-1, -1};
@@ -256,40 +257,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 else ++nvalid;
               }
             }
-            for (int c = 0; c < 9; ++c, ++n) {
-              const int sl = n % kSlots, u = n / kSlots;
-              if (u >= 1 && !tc::wait<false>(&bars[kBarCempty + sl], (u - 1) & 1, ab)) {
+            for (int t = 0; t < kSlots; ++t) {
+              if (m >= 1 && !tc::wait<false>(&bars[kBarCempty + t], (m - 1) & 1, ab)) {
                 ok = false;
                 break;
               }
-              uint8_t* dst = sm + kOffRing + sl * kSlotBytes;
-              uint64_t* fb = &bars[kBarCfull + sl];
+              uint8_t* dst = sm + kOffRing + t * kSlotBytes;
+              uint64_t* fb = &bars[kBarCfull + t];
               if (p.paged && nvalid < nh) {  // unreadable block: its rows count as zeros
                 for (int w = 0; w < nh; ++w)
-                  if (blk[w] < 0) {
-                    uint4* z = reinterpret_cast<uint4*>(dst + w * kChunkBytes);
-                    for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-                  }
+                  if (blk[w] < 0)
+                    for (int c = 0; c < 3; ++c) {
+                      uint4* z = reinterpret_cast<uint4*>(dst + c * kChunk128 + w * kChunkBytes);
+                      for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                    }
                 tc::fence_async_smem();
               }
               if (nvalid == 0) {
                 tc::mbar_arrive(fb);
                 continue;
               }
-              tc::mbar_expect_tx(fb, nvalid * kChunkBytes);
-              for (int w = 0; w < nh; ++w) {
-                if (p.paged) {
-                  if (blk[w] >= 0) tc::tma_load_3d(dst + w * kChunkBytes, &cache_map, c * 64, 0, blk[w], fb);
-                } else {
-                  tc::tma_load_3d(dst + w * kChunkBytes, &cache_map, c * 64, tt * kTile + 64 * w, s.b, fb);
+              tc::mbar_expect_tx(fb, 3 * nvalid * kChunkBytes);
+              for (int c = 0; c < 3; ++c) {
+                const int col = (3 * t + c) * 64;
+                for (int w = 0; w < nh; ++w) {
+                  uint8_t* d = dst + c * kChunk128 + w * kChunkBytes;
+                  if (p.paged) {
+                    if (blk[w] >= 0) tc::tma_load_3d(d, &cache_map, col, 0, blk[w], fb);
+                  } else {
+                    tc::tma_load_3d(d, &cache_map, col, tt * kTile + 64 * w, s.b, fb);
+                  }
                 }
               }
             }
+            // after this tile's own loads: warm L2 ahead.  The window opens one tile
+            // per tile (1, 2, 3, then kPrefetchTiles ahead): at launch every score CTA
+            // asks for its first tile at once, and a full window behind it would
+            // delay those bytes.
+            const int64_t want = min(hi, xg + 1 + min((int64_t)m + 1, (int64_t)kPrefetchTiles));
+            while (pf_next < want) prefetch_tile(pf_next++);
           }
         }
-        for (int k = 1; k <= kSlots && k <= n; ++k) {  // no copy in flight at exit
-          const int m = n - k;
-          tc::wait<false>(&bars[kBarCfull + m % kSlots], (m / kSlots) & 1, ab);
+        for (int k = 1; k <= kSlots && k <= m * kSlots; ++k) {  // no copy in flight at exit
+          const int u = m * kSlots - k;
+          tc::wait<false>(&bars[kBarCfull + u % kSlots], (u / kSlots) & 1, ab);
         }
       }
     } else if (warp == 1) {
@@ -298,7 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         constexpr uint32_t idS = tc::idesc_bf16(128, kTile, 0, 0);
         const uint32_t ring = smem_u32(sm + kOffRing);
         const uint32_t qrope = smem_u32(sm + kOffQrope);
-        int n = 0, m = 0, k = 0;
+        int m = 0, k = 0;
         bool ok = true;
         for (int64_t x = lo; x < hi && ok; ++k) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
@@ -312,30 +323,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc::tc_fence_after();
             const uint32_t dS = tb + kColS + (m & 1) * kTile;
-            // straight-line issue: per 64-column chunk one wait, four MMAs, one commit
+            // straight-line issue: per ring slot (three chunks) one wait, twelve MMAs, one commit
 #pragma unroll
-            for (int c = 0; c < 9; ++c) {
-              const int sl = (n + c) % kSlots;
-              if (!tc::wait<false>(&bars[kBarCfull + sl], ((n + c) / kSlots) & 1, ab)) {
+            for (int t = 0; t < kSlots; ++t) {
+              if (!tc::wait<false>(&bars[kBarCfull + t], m & 1, ab)) {
                 ok = false;
                 break;
               }
               tc::tc_fence_after();
-              const uint32_t sa = ring + sl * kSlotBytes;
-              if (c < 8) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  tc::mma_ts(dS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
-                             (c | kk) != 0 ? 1u : 0u);
-              } else {
+              for (int cc = 0; cc < 3; ++cc) {
+                const int c = 3 * t + cc;
+                const uint32_t sa = ring + t * kSlotBytes + cc * kChunk128;
+                if (c < 8) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  tc::mma_ss(dS, tc::smem_desc(qrope + kk * 32, 16, 1024), tc::smem_desc(sa + kk * 32, 16, 1024), idS,
-                             1u);
+                  for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ts(dS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
+                               (c | kk) != 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ss(dS, tc::smem_desc(qrope + kk * 32, 16, 1024), tc::smem_desc(sa + kk * 32, 16, 1024),
+                               idS, 1u);
+                }
               }
-              tc::mma_commit(&bars[kBarCempty + sl]);
+              tc::mma_commit(&bars[kBarCempty + t]);
             }
-            n += 9;
             if (ok) tc::mma_commit(&bars[kBarSfull + (m & 1)]);
           }
         }

@@ -315,6 +315,7 @@ static cudaError_t run(GemmArgs a, int groups, int ksplit, cudaStream_t s) {
 
 cudaError_t launch_absorb(const mla_dims& d, int batch, const void* q_c, const void* q_r,
                           const int32_t* pos, const void* w_uk, void* q_out, cudaStream_t s) {
+  if (proj_tc_supported(d, batch, true)) return launch_absorb_tc(d, batch, q_c, q_r, pos, w_uk, q_out, nullptr, s);
   GemmArgs a = {};
   const int D = d.d_latent + d.d_rope;
   a.M = batch;
@@ -343,6 +344,7 @@ cudaError_t launch_absorb(const mla_dims& d, int batch, const void* q_c, const v
 
 cudaError_t launch_out_proj(const mla_dims& d, int batch, const void* z, const void* w_uv,
                             void* o_out, cudaStream_t s) {
+  if (proj_tc_supported(d, batch, false)) return launch_out_proj_tc(d, batch, z, w_uv, o_out, nullptr, s);
   GemmArgs a = {};
   a.M = batch;
   a.N = d.d_v;
@@ -366,6 +368,9 @@ cudaError_t launch_append(const mla_dims& d, int n_tokens, int d_model, const vo
                           const void* w, const int32_t* seq_idx, const int32_t* pos, int n_seqs,
                           const int32_t* block_table, int max_blocks, int num_blocks,
                           int64_t seq_stride, void* pool, int32_t* status, cudaStream_t s) {
+  if (append_tc_supported(d, n_tokens, d_model))
+    return launch_append_tc(d, n_tokens, d_model, h, w, seq_idx, pos, n_seqs, block_table, max_blocks, num_blocks,
+                            seq_stride, pool, status, s);
   GemmArgs a = {};
   const int D = d.d_latent + d.d_rope;
   a.M = n_tokens;

@@ -64,6 +64,21 @@ bool tc_supported(const DecodeLaunch& a);
 cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
 size_t generic_smem_bytes(int D, int batch);
 
+// Tensor-core absorb / out-projection for d_h = d_v = 128, d_c = 512, d_R = 64
+// (absorb: batch <= 128, out-projection: batch <= 64).
+bool proj_tc_supported(const mla_dims& d, int batch, bool absorb);
+cudaError_t launch_absorb_tc(const mla_dims& d, int batch, const void* q_c, const void* q_r, const int32_t* pos,
+                             const void* w_uk, void* q_out, int32_t* status, cudaStream_t s);
+cudaError_t launch_out_proj_tc(const mla_dims& d, int batch, const void* z, const void* w_uv, void* o_out,
+                               int32_t* status, cudaStream_t s);
+
+// Tensor-core cache append for d_c = 512, d_R = 64, up to 32 tokens, d_model = 7168.
+bool append_tc_supported(const mla_dims& d, int n_tokens, int d_model);
+cudaError_t launch_append_tc(const mla_dims& d, int n_tokens, int d_model, const void* h, const void* w,
+                             const int32_t* seq_idx, const int32_t* pos, int n_seqs, const int32_t* block_table,
+                             int max_blocks, int num_blocks, int64_t seq_stride, void* pool, int32_t* status,
+                             cudaStream_t s);
+
 cudaError_t launch_absorb(const mla_dims& d, int batch, const void* q_c, const void* q_r,
                           const int32_t* pos, const void* w_uk, void* q_out, cudaStream_t s);
 cudaError_t launch_out_proj(const mla_dims& d, int batch, const void* z, const void* w_uv,

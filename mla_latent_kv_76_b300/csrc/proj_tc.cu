@@ -1,0 +1,562 @@
+// Tensor-core weight projections around decode, for the DeepSeek-V3 head
+// shape (d_h = d_v = 128, d_c = 512, d_R = 64):
+//   absorb    q~[b][i][n] = sum_k q^C[b][i][k] W^UK_i[k][n]   ("为什么矩阵吸收很关键":
+//             q^C.(W^UK c) = (q^C W^UK).c), plus q^R rotated into columns [512, 576)
+//   out-proj  o[b][i][v]  = sum_c z[b][i][c] W^UV_i[v][c]     (W^UV applied after the sum)
+// Both stream 16.8 MB of weights that are read exactly once; one CTA per head
+// TMA-loads its 128 KB weight matrix in one go and keeps it in shared memory.
+//
+// The batch is the MMA's M dimension (padded to 128): the activations' TMA
+// boxes hold only the real rows (a multiple of 8), packed back to back and
+// followed by the weights, so the MMA rows past the batch read other
+// operands' bytes and their results are simply not stored.  Operands use the
+// 128-byte-swizzled K-major layout (activations, W^UV) and MN-major layout
+// (W^UK, whose d_c columns are contiguous).
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kBox = 128 * 128;  // 64 bf16 x 128 rows
+
+struct ProjParams {
+  int batch, n_heads;
+  __nv_bfloat16* out;
+  int64_t out_sb, out_sh;  // element strides of batch and head in the output
+  // absorb only
+  const __nv_bfloat16* q_r;
+  const int32_t* pos;
+  float rope_base;
+};
+
+MLA_DEVI bool wait_done(uint64_t* b, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!tc::mbar_test(b, parity))
+    if (clock64() - t0 > tc::kWaitCycles) return false;
+  return true;
+}
+
+// The RoPE frequencies base^(-2i/64) in fp64 for i < 32, one pow per CTA.
+MLA_DEVI void rope_thetas(double* theta, float base, int tid) {
+  __shared__ double s_r;
+  if (tid == 0) s_r = pow((double)base, -2.0 / 64.0);
+  __syncthreads();
+  if (tid < 32) {
+    double t = 1.0, r = s_r;
+    for (int e = tid; e; e >>= 1) {
+      if (e & 1) t *= r;
+      r *= r;
+    }
+    theta[tid] = t;
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- absorb
+// smem: q^C boxes [2][rows8 x 128 B] at 0, then W^UK boxes [8][128 k x 128 B].
+__global__ void __launch_bounds__(kThreads, 1)
+    absorb_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                     const ProjParams p, int rows8, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ double theta[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x;
+  const int xbytes = rows8 * 128;
+  uint8_t* sx = sm;
+  uint8_t* sw = sm + ((2 * xbytes + 1023) & ~1023);
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  if (tid == 0) {
+    tc::prefetch_map(&map_w);
+    tc::prefetch_map(&map_x);
+    tc::mbar_expect_tx(&bars[0], 8 * kBox + 2 * xbytes);
+    for (int j = 0; j < 8; ++j) tc::tma_load_3d(sw + j * kBox, &map_w, 64 * j, 0, h, &bars[0]);
+    for (int j = 0; j < 2; ++j) tc::tma_load_3d(sx + j * xbytes, &map_x, 64 * j, h, 0, &bars[0]);
+  }
+  rope_thetas(theta, p.rope_base, tid);
+  bool ok = true;
+  if (tid == 0) {
+    ok = wait_done(&bars[0], 0);
+    if (ok) {
+      tc::tc_fence_after();
+      constexpr uint32_t id = tc::idesc_bf16(128, 256, 0, 1);
+      const uint32_t xa = smem_u32(sx), wa = smem_u32(sw);
+#pragma unroll
+      for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_ss(tb + nh * 256, tc::smem_desc(xa + (ks >> 2) * xbytes + (ks & 3) * 32, 16, 1024),
+                     tc::smem_desc(wa + nh * 4 * kBox + ks * 2048, kBox, 1024), id, ks > 0 ? 1u : 0u);
+      tc::mma_commit(&bars[1]);
+      ok = wait_done(&bars[1], 0);
+    }
+    if (!ok) report(status, MLA_ERR_DEVICE_TIMEOUT);
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  // ---- epilogue: thread = batch row; 512 accumulator columns -> bf16
+  const int b = warp * 32 + lane;
+  if (warp * 32 < p.batch) {
+    const uint32_t lane_t = tb + ((uint32_t)(warp * 32) << 16);
+    __nv_bfloat16* dst = p.out + (int64_t)b * p.out_sb + (int64_t)h * p.out_sh;
+#pragma unroll 1
+    for (int c = 0; c < 16; ++c) {
+      uint32_t r[32];
+      tc::tmem_ld32(lane_t + c * 32, r);
+      tc::tmem_wait_ld();
+      if (b < p.batch) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+      }
+    }
+  }
+  // ---- q^R part: RoPE(q^R, pos[b]) into columns [512, 576)
+  for (int idx = tid; idx < p.batch * 32; idx += kThreads) {
+    const int bb = idx >> 5, i = idx & 31;
+    const __nv_bfloat16* src = p.q_r + ((int64_t)bb * p.n_heads + h) * 64 + 2 * i;
+    const float x0 = __bfloat162float(src[0]), x1 = __bfloat162float(src[1]);
+    float c, sn;
+    rope_cos_sin_theta(p.pos[bb], theta[i], &c, &sn);
+    __nv_bfloat16* dst = p.out + (int64_t)bb * p.out_sb + (int64_t)h * p.out_sh + 512 + 2 * i;
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x0 * c - x1 * sn, x0 * sn + x1 * c);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tb, 512);
+  }
+}
+
+// ---------------------------------------------------------------- out-projection
+// smem: z boxes [8][rows8 x 128 B] at 0, then W^UV boxes [8][128 v x 128 B].
+__global__ void __launch_bounds__(kThreads, 1)
+    out_proj_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                       const ProjParams p, int rows8, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x;
+  const int xbytes = rows8 * 128;
+  uint8_t* sx = sm;
+  uint8_t* sw = sm + ((8 * xbytes + 1023) & ~1023);
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  if (tid == 0) {
+    tc::prefetch_map(&map_w);
+    tc::prefetch_map(&map_x);
+    tc::mbar_expect_tx(&bars[0], 8 * kBox + 8 * xbytes);
+    for (int j = 0; j < 8; ++j) tc::tma_load_3d(sw + j * kBox, &map_w, 64 * j, 0, h, &bars[0]);
+    for (int j = 0; j < 8; ++j) tc::tma_load_3d(sx + j * xbytes, &map_x, 64 * j, h, 0, &bars[0]);
+    bool ok = wait_done(&bars[0], 0);
+    if (ok) {
+      tc::tc_fence_after();
+      constexpr uint32_t id = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t xa = smem_u32(sx), wa = smem_u32(sw);
+#pragma unroll
+      for (int ks = 0; ks < 32; ++ks)
+        tc::mma_ss(tb, tc::smem_desc(xa + (ks >> 2) * xbytes + (ks & 3) * 32, 16, 1024),
+                   tc::smem_desc(wa + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024), id, ks > 0 ? 1u : 0u);
+      tc::mma_commit(&bars[1]);
+      ok = wait_done(&bars[1], 0);
+    }
+    if (!ok) report(status, MLA_ERR_DEVICE_TIMEOUT);
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  const int b = warp * 32 + lane;
+  if (warp * 32 < p.batch) {
+    const uint32_t lane_t = tb + ((uint32_t)(warp * 32) << 16);
+    __nv_bfloat16* dst = p.out + (int64_t)b * p.out_sb + (int64_t)h * p.out_sh;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      tc::tmem_ld32(lane_t + c * 32, r);
+      tc::tmem_wait_ld();
+      if (b < p.batch) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tb, 128);
+  }
+}
+
+
+// ---------------------------------------------------------------- cache append
+// [c; k^R] = [W^DKV; W^KR] h for up to 32 new tokens ("MLA 的核心结构": c^KV =
+// W^DKV h; "RoPE 为什么要解耦": k^R = RoPE(W^KR h)), tokens as M (padded to 128).
+// A cluster of kAppendSplit CTAs shares one 96-column slice of the 576 outputs,
+// each CTA one 448-deep slice of d_model (7 boxes of 64): 6 x 16 = 96 CTAs
+// stream the 8.3 MB weight once, all of it in flight at the same time.  The
+// fp32 partial tiles are summed in rank order through distributed shared
+// memory, each rank finishing 6 of the 96 columns: RoPE on the k^R pairs,
+// bf16 rounding, and the write into the cache slot of (sequence, position).
+constexpr int kAppendSplit = 16;
+MLA_DEVI float ld_cluster_f32(uint32_t a) {
+  float x;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(a) : "memory");
+  return x;
+}
+constexpr int kAppendN = 96;
+constexpr int kAppendKBoxes = 7;
+
+struct AppendParams {
+  int n_tokens, d_model;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  int n_seqs;
+  const int32_t* block_table;
+  int max_blocks, num_blocks, block_tokens;
+  int64_t seq_stride;
+  __nv_bfloat16* pool;
+  float rope_base;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    append_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+                     const AppendParams p, int rows8) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ double theta[32];
+  __shared__ float red[kAppendN * 32];  // this CTA's partial tile, [column][token t < 32]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = tc::cluster_rank();
+  const int ntile = (int)(blockIdx.x / kAppendSplit);
+  const int n0 = ntile * kAppendN;
+  const int k0 = (int)rank * kAppendKBoxes * 64;
+  const int hbytes = rows8 * 128;
+  const int wbytes = kAppendN * 128;
+  uint8_t* sh = sm;                                                    // [7][rows8 x 128 B]
+  uint8_t* sw = sm + ((kAppendKBoxes * hbytes + 1023) & ~1023);        // [7][96 x 128 B]
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  if (tid == 0) {
+    tc::prefetch_map(&map_w);
+    tc::prefetch_map(&map_h);
+    tc::mbar_expect_tx(&bars[0], kAppendKBoxes * (wbytes + hbytes));
+    for (int j = 0; j < kAppendKBoxes; ++j) {
+      tc::tma_load_2d(sw + j * wbytes, &map_w, k0 + 64 * j, n0, &bars[0]);
+      tc::tma_load_2d(sh + j * hbytes, &map_h, k0 + 64 * j, 0, &bars[0]);
+    }
+    bool ok = wait_done(&bars[0], 0);
+    if (ok) {
+      tc::tc_fence_after();
+      constexpr uint32_t id = tc::idesc_bf16(128, kAppendN, 0, 0);
+      const uint32_t ha = smem_u32(sh), wa = smem_u32(sw);
+#pragma unroll
+      for (int ks = 0; ks < 4 * kAppendKBoxes; ++ks)
+        tc::mma_ss(tb, tc::smem_desc(ha + (ks >> 2) * hbytes + (ks & 3) * 32, 16, 1024),
+                   tc::smem_desc(wa + (ks >> 2) * wbytes + (ks & 3) * 32, 16, 1024), id, ks > 0 ? 1u : 0u);
+      tc::mma_commit(&bars[1]);
+      ok = wait_done(&bars[1], 0);
+    }
+    if (!ok) report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+  }
+  rope_thetas(theta, p.rope_base, tid);  // contains __syncthreads
+  tc::tc_fence_after();
+  __syncwarp();
+  if (warp == 0) {  // token rows t < 32 live in TMEM lanes 0..31
+    uint32_t r[32];
+#pragma unroll
+    for (int c = 0; c < kAppendN / 32; ++c) {
+      tc::tmem_ld32(tb + c * 32, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) red[(c * 32 + i) * 32 + lane] = __uint_as_float(r[i]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();
+  // rank r finishes columns [n0 + 6 r, n0 + 6 r + 6) of every token: sum the 16
+  // partials in rank order, RoPE the k^R pairs, round, scatter into the cache
+  constexpr int kCols = kAppendN / kAppendSplit;
+  for (int idx = tid; idx < p.n_tokens * (kCols / 2); idx += kThreads) {
+    const int t = idx / (kCols / 2), cp = idx % (kCols / 2);
+    const int cl = (int)rank * kCols + 2 * cp;  // local column (even)
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < kAppendSplit; ++q) {
+      v0 += ld_cluster_f32(tc::map_peer(&red[cl * 32 + t], (uint32_t)q));
+      v1 += ld_cluster_f32(tc::map_peer(&red[(cl + 1) * 32 + t], (uint32_t)q));
+    }
+    const int n = n0 + cl;
+    const int s = p.seq_idx[t], ps = p.pos[t];
+    bool ok = (s >= 0) && (s < p.n_seqs) && (ps >= 0);
+    int64_t row = 0;
+    if (ok) {
+      if (p.block_table) {
+        const int lb = ps / p.block_tokens;
+        ok = lb < p.max_blocks;
+        if (ok) {
+          const int blk = p.block_table[(int64_t)s * p.max_blocks + lb];
+          ok = (blk >= 0) && (blk < p.num_blocks);
+          row = (int64_t)blk * p.block_tokens + ps % p.block_tokens;
+        }
+      } else {
+        ok = ps < p.seq_stride;
+        row = (int64_t)s * p.seq_stride + ps;
+      }
+    }
+    if (!ok) {
+      report(p.status, MLA_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    if (n >= 512) {
+      float c, sn;
+      rope_cos_sin_theta(ps, theta[(n - 512) >> 1], &c, &sn);
+      const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
+      v0 = r0;
+      v1 = r1;
+    }
+    *reinterpret_cast<uint32_t*>(p.pool + row * 576 + n) = pack_bf16x2(v0, v1);
+  }
+  tc::cluster_sync();  // peers keep their partials until every rank has read them
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tb, 128);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map, 128-byte swizzle, box {64, box1, box2}.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+              uint64_t s2_bytes, uint32_t box1, uint32_t box2) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  const cuuint32_t box[3] = {64, box1, box2}, es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 tensor map, 128-byte swizzle, box {64, box1}.
+bool make_map2(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t s1_bytes, uint32_t box1) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {d0, d1};
+  const cuuint64_t strides[1] = {s1_bytes};
+  const cuuint32_t box[2] = {64, box1}, es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int append_smem_bytes(int rows8) {
+  return ((kAppendKBoxes * rows8 * 128 + 1023) & ~1023) + kAppendKBoxes * kAppendN * 128 + 1024;
+}
+
+// True when a cluster of 16 CTAs of the append kernel can be resident on this
+// device (a non-portable cluster size: it needs 16 free SMs in one GPC).
+// Decided once per device; also sets the kernel's attributes there.
+bool append_cluster_fits() {
+  static int fits_dev[64];  // 0 unknown, 1 no, 2 yes
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  int& fits = fits_dev[dev];
+  if (fits) return fits == 2;
+  fits = 1;
+  const int smem = append_smem_bytes(32);
+  if (cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+      cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((576 / kAppendN) * kAppendSplit);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kAppendSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, append_tc_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  fits = n >= 1 ? 2 : 1;
+  return fits == 2;
+}
+
+bool append_tc_supported(const mla_dims& d, int n_tokens, int d_model) {
+  return d.d_latent == 512 && d.d_rope == 64 && n_tokens >= 1 && n_tokens <= 32 &&
+         d_model == kAppendSplit * kAppendKBoxes * 64 && append_cluster_fits();
+}
+
+cudaError_t launch_append_tc(const mla_dims& d, int n_tokens, int d_model, const void* h, const void* w,
+                             const int32_t* seq_idx, const int32_t* pos, int n_seqs, const int32_t* block_table,
+                             int max_blocks, int num_blocks, int64_t seq_stride, void* pool, int32_t* status,
+                             cudaStream_t s) {
+  const int rows8 = (n_tokens + 7) & ~7;
+  CUtensorMap mw, mh;
+  if (!make_map2(&mw, w, (uint64_t)d_model, 576, (uint64_t)d_model * 2, kAppendN) ||
+      !make_map2(&mh, h, (uint64_t)d_model, (uint64_t)n_tokens, (uint64_t)d_model * 2, rows8))
+    return cudaErrorInvalidValue;
+  AppendParams p;
+  p.n_tokens = n_tokens;
+  p.d_model = d_model;
+  p.seq_idx = seq_idx;
+  p.pos = pos;
+  p.n_seqs = n_seqs;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.block_tokens = d.block_tokens;
+  p.seq_stride = seq_stride;
+  p.pool = static_cast<__nv_bfloat16*>(pool);
+  p.rope_base = d.rope_base;
+  p.status = status;
+  const int smem = append_smem_bytes(rows8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((576 / kAppendN) * kAppendSplit);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kAppendSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, append_tc_kernel, mw, mh, p, rows8);
+}
+
+bool proj_tc_supported(const mla_dims& d, int batch, bool absorb) {
+  if (d.d_latent != 512 || batch < 1) return false;
+  if (absorb) return d.d_head == 128 && d.d_rope == 64 && batch <= 128;
+  return d.d_v == 128 && batch <= 64;
+}
+
+cudaError_t launch_absorb_tc(const mla_dims& d, int batch, const void* q_c, const void* q_r, const int32_t* pos,
+                             const void* w_uk, void* q_out, int32_t* status, cudaStream_t s) {
+  const int rows8 = (batch + 7) & ~7;
+  CUtensorMap mw, mx;
+  // W^UK [h][k][n]: dims {n 512, k 128, h}
+  if (!make_map(&mw, w_uk, 512, 128, (uint64_t)d.n_heads, 512 * 2, (uint64_t)128 * 512 * 2, 128, 1) ||
+      // q^C [b][h][k]: dims {k 128, h, b}
+      !make_map(&mx, q_c, 128, (uint64_t)d.n_heads, (uint64_t)batch, 128 * 2, (uint64_t)d.n_heads * 128 * 2, 1,
+                rows8))
+    return cudaErrorInvalidValue;
+  ProjParams p;
+  p.batch = batch;
+  p.n_heads = d.n_heads;
+  p.out = static_cast<__nv_bfloat16*>(q_out);
+  p.out_sb = (int64_t)d.n_heads * 576;
+  p.out_sh = 576;
+  p.q_r = static_cast<const __nv_bfloat16*>(q_r);
+  p.pos = pos;
+  p.rope_base = d.rope_base;
+  const int smem = ((2 * rows8 * 128 + 1023) & ~1023) + 8 * kBox + 1024;
+  cudaError_t e = ensure_smem<absorb_tc_kernel>(smem);
+  if (e != cudaSuccess) return e;
+  absorb_tc_kernel<<<d.n_heads, kThreads, smem, s>>>(mw, mx, p, rows8, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_out_proj_tc(const mla_dims& d, int batch, const void* z, const void* w_uv, void* o_out,
+                               int32_t* status, cudaStream_t s) {
+  const int rows8 = (batch + 7) & ~7;
+  CUtensorMap mw, mx;
+  // W^UV [h][v][c]: dims {c 512, v 128, h}
+  if (!make_map(&mw, w_uv, 512, 128, (uint64_t)d.n_heads, 512 * 2, (uint64_t)128 * 512 * 2, 128, 1) ||
+      // z [b][h][c]: dims {c 512, h, b}
+      !make_map(&mx, z, 512, (uint64_t)d.n_heads, (uint64_t)batch, 512 * 2, (uint64_t)d.n_heads * 512 * 2, 1,
+                rows8))
+    return cudaErrorInvalidValue;
+  ProjParams p = {};
+  p.batch = batch;
+  p.n_heads = d.n_heads;
+  p.out = static_cast<__nv_bfloat16*>(o_out);
+  p.out_sb = (int64_t)d.n_heads * 128;
+  p.out_sh = 128;
+  const int smem = ((8 * rows8 * 128 + 1023) & ~1023) + 8 * kBox + 1024;
+  cudaError_t e = ensure_smem<out_proj_tc_kernel>(smem);
+  if (e != cudaSuccess) return e;
+  out_proj_tc_kernel<<<d.n_heads, kThreads, smem, s>>>(mw, mx, p, rows8, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -278,6 +278,37 @@ def test_append_values_and_bounds(mla):
     assert np.array_equal(dev_to_bits(pool), before)
 
 
+@pytest.mark.parametrize("n_tok,paged", [(1, True), (7, False), (16, True), (31, False), (32, True), (33, False)])
+def test_append_at_model_width(mla, n_tok, paged):
+    """d_model = 7168 (the DeepSeek-V3 hidden size): up to 32 tokens take the
+    tensor-core kernel (cluster split of d_model), more take the CUDA-core
+    GEMM.  Written rows against the fp64 oracle, every other row untouched."""
+    rng = np.random.default_rng(100 + n_tok)
+    lens = rng.integers(1, 700, size=n_tok)
+    wl = mi.make_random(200 + n_tok, 4, 512, 64, lens, paged=paged, poison=False, d_model=7168)
+    dims = mla.Dims.of(wl)
+    pool = bits_to_dev(wl.pool)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_append_cache(dims, bits_to_dev(wl.h), bits_to_dev(wl.w_dkv_kr), i32(wl.app_seq), i32(wl.app_pos),
+                         pool, n_seqs=wl.batch, block_table=i32(wl.block_table) if paged else None,
+                         num_blocks=wl.num_blocks, seq_stride=wl.seq_stride, dev_status=status)
+    torch.cuda.synchronize()
+    assert mla.mla_read_status(status) == 0
+    got = dev_to_bits(pool).reshape(-1, wl.row_dim)
+    want = orc.append_cache(wl.pool, wl.h, wl.w_dkv_kr, wl.app_seq, wl.app_pos, wl.d_latent,
+                            wl.block_table if paged else None, 64, wl.seq_stride, wl.rope_base).reshape(-1, wl.row_dim)
+    if paged:
+        flat = wl.block_table[wl.app_seq, wl.app_pos // 64].astype(np.int64) * 64 + wl.app_pos % 64
+    else:
+        flat = wl.app_seq.astype(np.int64) * wl.seq_stride + wl.app_pos
+    others = np.ones(got.shape[0], dtype=bool)
+    others[flat] = False
+    assert np.array_equal(got[others], want[others])
+    exact = orc.append_rows(orc.bf16_to_f64(wl.h), orc.bf16_to_f64(wl.w_dkv_kr), wl.app_pos, wl.d_latent,
+                            wl.rope_base)
+    assert_bf16_gemm(got[flat], exact, append_abs_terms(wl.h, wl.w_dkv_kr, wl.d_latent), "append")
+
+
 @pytest.mark.parametrize("B", [1, 16, 40, 256])
 def test_absorb_and_out_proj(mla, B):
     rng = np.random.default_rng(B)
