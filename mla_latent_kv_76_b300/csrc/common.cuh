@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "../../include/mla.h"
 
 #define MLA_DEVI __device__ __forceinline__
@@ -63,17 +65,43 @@ MLA_DEVI uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- RoPE
-// cos/sin of pos * theta with theta = base^(-2i/d_R) given in fp64.  The
-// angle is formed and reduced modulo 2*pi in fp64 (positions reach 1e5 and
-// more, where an fp32 angle would be off by ~1e-2 rad), then evaluated with
-// the fp32 sincosf on [0, 2*pi).
-MLA_DEVI void rope_cos_sin_theta(int pos, double theta, float* c, float* s) {
+// Frequency i of the rotary embedding as turns per position,
+// u_i = base^(-2i/d_R) / (2 pi), held as an fp32 pair hi + lo (about 48 bits).
+// It is computed on the host in fp64: this part runs fp64 arithmetic at a tiny
+// fraction of its fp32 rate (one device pow() cost ~4 us per CTA).
+struct RopeTurns {
+  float hi[64];
+  float lo[64];
+};
+
+inline void rope_turns_host(float base, int d_rope, RopeTurns* t) {
   const double two_pi = 6.283185307179586476925286766559;
-  const double inv_two_pi = 0.15915494309189533576888376337251;
-  const double ang = (double)pos * theta;
-  const double k = floor(ang * inv_two_pi);
-  const double r = fma(-k, two_pi, ang);
-  sincosf((float)r, s, c);
+  for (int i = 0; i < 64; ++i) {
+    const double u = (2 * i < d_rope) ? std::pow((double)base, -2.0 * i / d_rope) / two_pi : 0.0;
+    t->hi[i] = (float)u;
+    t->lo[i] = (float)(u - (double)t->hi[i]);
+  }
+}
+
+// frac(x * (a_hi + a_lo)) for an integer-valued x < 2^24, in fp32: the product's
+// rounding error is recovered exactly with an fma, and p - floor(p) is exact.
+MLA_DEVI float turns_frac(float x, float a_hi, float a_lo) {
+  const float p = x * a_hi;
+  const float e = fmaf(x, a_hi, -p);
+  const float f = p - floorf(p);
+  const float g = f + fmaf(x, a_lo, e);
+  return g - floorf(g);
+}
+
+// cos/sin of pos * theta_i.  The angle is reduced in turns (positions are split
+// as pos = 4096 ph + pl so both factors are exact in fp32); the angle error stays
+// below 1e-5 rad for every int32 position, far under a bf16 step, where a plain
+// fp32 pos * theta would be off by ~1e-2 rad at pos ~ 1e5.
+MLA_DEVI void rope_cos_sin(int pos, float u_hi, float u_lo, float* c, float* s) {
+  const float ph = (float)(pos >> 12), pl = (float)(pos & 4095);
+  float t = turns_frac(ph, u_hi * 4096.f, u_lo * 4096.f) + turns_frac(pl, u_hi, u_lo);
+  t -= floorf(t);
+  sincospif(2.f * t, s, c);
 }
 
 // Row stride in bytes for a bf16 row of `elems` values staged for ldmatrix:

@@ -20,15 +20,21 @@
 // re-reads the latent columns a few microseconds later, from L2.
 //
 // Score CTA, 384 threads: warp 0 TMA (3 ring slots, each three 64-column
-// chunks of 128 tokens, 128-byte swizzle), warp 1 MMA issue (S double-buffered
+// chunks of 128 tokens, 128-byte swizzle; lane c issues chunk c), warp 1 MMA issue (S double-buffered
 // in TMEM; one barrier wait and one commit per 12 MMAs),
 // warps 4-7 / 8-11 softmax for token columns 0-63 / 64-127 (thread = head),
 // warps 2 / 3 ship each warpgroup's P to the value CTA as one bulk copy.
-// Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns), warp 1 MMA,
+// Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns; lane c issues
+// column chunk c), warp 1 MMA,
 // warps 2-3 zero the rows past the sequence end in the last half tile (NaN
 // garbage must not meet a zero weight), warps 4-7 rescale O and write the
 // segment's partial (thread = head), warp 8 returns P buffers to the score CTA
 // once O has consumed them, warp 9 frees the score CTA's staging once P landed.
+//
+// Copies are issued from several lanes because one issuing thread keeps only
+// one or two bulk copies moving at a time (measured on B300: ~30 GB/s per
+// thread with 8 KB copies, ~85 GB/s with four issuers), far below what an SM
+// can take in.
 //
 // Online softmax with a lazily updated reference maximum m_ref (base 2):
 // P = 2^(x - m_ref); m_ref moves, and O and l are rescaled, only when a tile's
@@ -51,7 +57,6 @@ constexpr int kTile = 128;           // tokens per score tile (two 64-token halv
 constexpr int kThreads = 384;
 constexpr int kTcMaxBatch = 1024;
 constexpr float kRescaleThreshold = 16.f;
-constexpr int kPrefetchTiles = 4;    // the score CTA's producer warms L2 this many tiles ahead
 
 // ---- P hand-off unit: 64 tokens of bf16 weights for 128 heads, then metadata
 constexpr int kPBytes = kH * 128;                  // 128 heads x 64 tokens bf16 (SW128 K-major)
@@ -147,7 +152,8 @@ MLA_DEVI int half_block(const TcParams& p, const Seg& s, int tt, int w) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map, const TcParams p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map, const __grid_constant__ CUtensorMap cache_map128,
+                     const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -164,7 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     if (rank == 0) {
       for (int i = 0; i < kSlots; ++i) {
-        tc::mbar_init(&bars[kBarCfull + i], 1);
+        tc::mbar_init(&bars[kBarCfull + i], 3);  // one arrival per issuing lane
         tc::mbar_init(&bars[kBarCempty + i], 1);
       }
       for (int i = 0; i < 2; ++i) {
@@ -181,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[kBarLsum], 256);
     } else {
       for (int i = 0; i < kVStages; ++i) {
-        tc::mbar_init(&bars[kBarFull + i], 1);
+        tc::mbar_init(&bars[kBarFull + i], 8);  // one arrival per issuing lane
         tc::mbar_init(&bars[kBarEmpty + i], 1 + 64);
         tc::mbar_init(&bars[kBarFix + i], 64);
       }
@@ -212,96 +218,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (rank == 0) {
     // ================================================================ score CTA
     if (warp == 0) {
-      if (lane == 0) {
-        // ---------------------------------------------------------- TMA producer
-        tc::prefetch_map(&cache_map);
+      if (lane < 3 * kSlots) {
+        // ---------------------------------------------------------- TMA producer, lane c = column chunk c
+        // (ring slot c / 3).  One issuing thread keeps only one or two copies moving,
+        // so every chunk of a tile has its own issuing lane.
+        const int c = lane, t = c / 3;
+        if (c == 0) {
+          tc::prefetch_map(&cache_map);
+          tc::prefetch_map(&cache_map128);
+        }
+        uint8_t* dst = sm + kOffRing + t * kSlotBytes + (c % 3) * kChunk128;
+        uint64_t* fb = &bars[kBarCfull + t];
         bool ok = true;
-        // The ring holds ~1 tile, less than HBM latency covers at full rate: tiles
-        // kPrefetchTiles ahead are pulled into L2 first, so the ring loads hit L2.
-        auto prefetch_tile = [&](int64_t xt) {
-          const int b = seq_of_tile(pre, B, xt);
-          const int tt = (int)(xt - pre[b]);
-          const int L = effective_len(p.seqlens, b, cap, nullptr);
-          const int nh = min(2, (L - tt * kTile + 63) >> 6);
-          for (int w = 0; w < nh; ++w) {
-            const int rows = min(64, L - tt * kTile - 64 * w);
-            const __nv_bfloat16* src;
-            if (p.paged) {
-              const int lb = 2 * tt + w;
-              if (lb >= p.max_blocks) continue;
-              const int blk = p.block_table[(int64_t)b * p.max_blocks + lb];
-              if (blk < 0 || blk >= p.num_blocks) continue;
-              src = p.pool + (int64_t)blk * 64 * kD;
-            } else {
-              src = p.pool + ((int64_t)b * p.seq_stride + tt * kTile + 64 * w) * kD;
-            }
-            tc::prefetch_l2(src, (uint32_t)rows * kD * 2);
-          }
-        };
-        int64_t xg = lo;           // global index of the tile being loaded
-        int64_t pf_next = lo + 1;  // next tile to warm in L2
-        int m = 0;                 // tiles loaded so far
+        int m = 0;  // tiles loaded so far
         for (int64_t x = lo; x < hi && ok;) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
           x += s.ntile;
-          for (int j = 0; j < s.ntile && ok; ++j, ++xg, ++m) {
+          for (int j = 0; j < s.ntile; ++j, ++m) {
             const int tt = s.t_begin + j;
-            const int nh = halves_of(s, tt);
-            int blk[2] = {-1, -1};
-            int nvalid = nh;
+            if (m >= 1 && !tc::wait<false>(&bars[kBarCempty + t], (m - 1) & 1, ab)) {
+              ok = false;
+              break;
+            }
             if (p.paged) {
-              nvalid = 0;
+              const int nh = halves_of(s, tt);
+              int blk[2] = {-1, -1};
+              int nvalid = 0;
               for (int w = 0; w < nh; ++w) {
                 blk[w] = half_block(p, s, tt, w);
-                if (blk[w] < 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
-                else ++nvalid;
+                if (blk[w] < 0) {
+                  if (c == 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
+                  // unreadable block: its rows count as zeros
+                  uint4* z = reinterpret_cast<uint4*>(dst + w * kChunkBytes);
+                  for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                } else {
+                  ++nvalid;
+                }
               }
-            }
-            for (int t = 0; t < kSlots; ++t) {
-              if (m >= 1 && !tc::wait<false>(&bars[kBarCempty + t], (m - 1) & 1, ab)) {
-                ok = false;
-                break;
-              }
-              uint8_t* dst = sm + kOffRing + t * kSlotBytes;
-              uint64_t* fb = &bars[kBarCfull + t];
-              if (p.paged && nvalid < nh) {  // unreadable block: its rows count as zeros
-                for (int w = 0; w < nh; ++w)
-                  if (blk[w] < 0)
-                    for (int c = 0; c < 3; ++c) {
-                      uint4* z = reinterpret_cast<uint4*>(dst + c * kChunk128 + w * kChunkBytes);
-                      for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-                    }
-                tc::fence_async_smem();
-              }
+              if (nvalid < nh) tc::fence_async_smem();
               if (nvalid == 0) {
                 tc::mbar_arrive(fb);
                 continue;
               }
-              tc::mbar_expect_tx(fb, 3 * nvalid * kChunkBytes);
-              for (int c = 0; c < 3; ++c) {
-                const int col = (3 * t + c) * 64;
-                for (int w = 0; w < nh; ++w) {
-                  uint8_t* d = dst + c * kChunk128 + w * kChunkBytes;
-                  if (p.paged) {
-                    if (blk[w] >= 0) tc::tma_load_3d(d, &cache_map, col, 0, blk[w], fb);
-                  } else {
-                    tc::tma_load_3d(d, &cache_map, col, tt * kTile + 64 * w, s.b, fb);
-                  }
-                }
-              }
+              tc::mbar_expect_tx(fb, nvalid * kChunkBytes);
+              for (int w = 0; w < nh; ++w)
+                if (blk[w] >= 0) tc::tma_load_3d(dst + w * kChunkBytes, &cache_map, c * 64, 0, blk[w], fb);
+            } else {
+              // contiguous cache: one 128-row box per 64-column chunk (rows past the
+              // sequence are masked by the softmax; past the allocation they read as zero)
+              tc::mbar_expect_tx(fb, kChunk128);
+              tc::tma_load_3d(dst, &cache_map128, c * 64, tt * kTile, s.b, fb);
             }
-            // after this tile's own loads: warm L2 ahead.  The window opens one tile
-            // per tile (1, 2, 3, then kPrefetchTiles ahead): at launch every score CTA
-            // asks for its first tile at once, and a full window behind it would
-            // delay those bytes.
-            const int64_t want = min(hi, xg + 1 + min((int64_t)m + 1, (int64_t)kPrefetchTiles));
-            while (pf_next < want) prefetch_tile(pf_next++);
           }
         }
-        for (int k = 1; k <= kSlots && k <= m * kSlots; ++k) {  // no copy in flight at exit
-          const int u = m * kSlots - k;
-          tc::wait<false>(&bars[kBarCfull + u % kSlots], (u / kSlots) & 1, ab);
-        }
+        if (m >= 1) tc::wait<false>(fb, (m - 1) & 1, ab);  // no copy in flight at exit
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -518,9 +488,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ================================================================ value CTA
     if (warp == 0) {
-      if (lane == 0) {
-        // ---------------------------------------------------------- TMA producer
-        tc::prefetch_map(&cache_map);
+      if (lane < 8) {
+        // ---------------------------------------------------------- TMA producer, lane c = column chunk c
+        const int c = lane;
+        if (c == 0) tc::prefetch_map(&cache_map);
         int hh = 0;
         bool ok = true;
         for (int64_t x = lo; x < hi && ok;) {
@@ -535,28 +506,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              uint8_t* dst = sm + kOffStage + st * kVStageBytes;
+              uint8_t* dst = sm + kOffStage + st * kVStageBytes + c * kChunkBytes;
               uint64_t* fb = &bars[kBarFull + st];
               if (p.paged) {
                 const int blk = half_block(p, s, tt, w);
                 if (blk < 0) {
                   uint4* z = reinterpret_cast<uint4*>(dst);
-                  for (int i = 0; i < kVStageBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                  for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
                   tc::fence_async_smem();
                   tc::mbar_arrive(fb);
                   continue;
                 }
-                tc::mbar_expect_tx(fb, kVStageBytes);
-                for (int c = 0; c < 8; ++c) tc::tma_load_3d(dst + c * kChunkBytes, &cache_map, c * 64, 0, blk, fb);
+                tc::mbar_expect_tx(fb, kChunkBytes);
+                tc::tma_load_3d(dst, &cache_map, c * 64, 0, blk, fb);
               } else {
-                tc::mbar_expect_tx(fb, kVStageBytes);
-                for (int c = 0; c < 8; ++c)
-                  tc::tma_load_3d(dst + c * kChunkBytes, &cache_map, c * 64, tt * kTile + 64 * w, s.b, fb);
+                tc::mbar_expect_tx(fb, kChunkBytes);
+                tc::tma_load_3d(dst, &cache_map, c * 64, tt * kTile + 64 * w, s.b, fb);
               }
             }
           }
         }
-        for (int k = 1; k <= kVStages && k <= hh; ++k) {
+        for (int k = 1; k <= kVStages && k <= hh; ++k) {  // no copy in flight at exit
           const int m = hh - k;
           tc::wait<false>(&bars[kBarFull + m % kVStages], (m / kVStages) & 1, ab);
         }
@@ -879,6 +849,15 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // the score CTA's whole-tile boxes (contiguous cache only)
+  CUtensorMap map128 = map;
+  if (!a.block_table) {
+    const cuuint32_t box128[3] = {64, 128, 1};
+    if (enc(&map128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.pool), dims, strides, box128, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   TcParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.pool = static_cast<const __nv_bfloat16*>(a.pool);
@@ -898,7 +877,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(a.batch);
   cudaError_t e = ensure_smem<decode_tc_kernel>((int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, p);
+  decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, map128, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 grid(kDC / 32, a.batch);

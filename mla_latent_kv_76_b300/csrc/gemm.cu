@@ -36,7 +36,7 @@ struct GemmArgs {
   const __nv_bfloat16* q_r;
   const int32_t* pos;
   int n_heads, d_rope, d_latent;
-  float rope_base;
+  RopeTurns rope;
   // append
   const int32_t* seq_idx;
   int n_seqs;
@@ -65,13 +65,12 @@ struct GemmCfg {
 };
 
 template <int BM, int BN, int BK, int STAGES, WLayout WL, Epi EP>
-__global__ void __launch_bounds__(128) sgemm_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(128) sgemm_kernel(const __grid_constant__ GemmArgs a) {
   using C = GemmCfg<BM, BN, BK, STAGES, WL>;
   constexpr int WN = BN / 4;  // output columns per warp
   constexpr int NB = WN / 8;  // n8 blocks per warp
   static_assert(WN % 8 == 0, "BN must be a multiple of 32");
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ double s_theta[64];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ks = a.ksplit;
@@ -213,24 +212,6 @@ __global__ void __launch_bounds__(128) sgemm_kernel(const GemmArgs a) {
   }
 
   // ------------------------------------------------------------ epilogue
-  // RoPE frequencies theta_i = base^(-2i/d_R) in fp64, only in CTAs that rotate
-  // something: one pow for r = base^(-2/d_R), then theta_i = r^i by squaring
-  // (FP64 throughput is low on this part; 32 pows per CTA would dominate).
-  const bool needs_theta = (EP == Epi::APPEND && n0 + BN > a.d_latent) || (EP == Epi::ABSORB && blockIdx.x == 0);
-  if (needs_theta) {
-    __shared__ double s_r;
-    if (tid == 0) s_r = pow((double)a.rope_base, -2.0 / (double)a.d_rope);
-    __syncthreads();
-    for (int i = tid; i < a.d_rope / 2 && i < 64; i += 128) {
-      double t = 1.0, base = s_r;
-      for (int e = i; e; e >>= 1) {
-        if (e & 1) t *= base;
-        base *= base;
-      }
-      s_theta[i] = t;
-    }
-    __syncthreads();
-  }
   for (int i = tid; i < BM * (BN / 2); i += 128) {
     const int r = i / (BN / 2), cp = i % (BN / 2);
     const int m = m0 + r, n = n0 + 2 * cp;
@@ -263,7 +244,8 @@ __global__ void __launch_bounds__(128) sgemm_kernel(const GemmArgs a) {
       dst_row = a.Y + row * a.y_sm;
       if (n >= a.d_latent) {
         float c, sn;
-        rope_cos_sin_theta(p, s_theta[(n - a.d_latent) >> 1], &c, &sn);
+        const int fi = (n - a.d_latent) >> 1;
+        rope_cos_sin(p, a.rope.hi[fi], a.rope.lo[fi], &c, &sn);
         const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
         v0 = r0;
         v1 = r1;
@@ -283,7 +265,7 @@ __global__ void __launch_bounds__(128) sgemm_kernel(const GemmArgs a) {
       const __nv_bfloat16* src = a.q_r + ((int64_t)m * a.n_heads + g) * a.d_rope + 2 * i;
       const float x0 = __bfloat162float(src[0]), x1 = __bfloat162float(src[1]);
       float c, sn;
-      rope_cos_sin_theta(a.pos[m], s_theta[i], &c, &sn);
+      rope_cos_sin(a.pos[m], a.rope.hi[i], a.rope.lo[i], &c, &sn);
       __nv_bfloat16* dst = a.Y + g * a.y_sg + m * a.y_sm + a.d_latent + 2 * i;
       *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x0 * c - x1 * sn, x0 * sn + x1 * c);
     }
@@ -335,7 +317,7 @@ cudaError_t launch_absorb(const mla_dims& d, int batch, const void* q_c, const v
   a.n_heads = d.n_heads;
   a.d_rope = d.d_rope;
   a.d_latent = d.d_latent;
-  a.rope_base = d.rope_base;
+  rope_turns_host(d.rope_base, d.d_rope, &a.rope);
   // K = d_h is short: one CTA per (head, 128 latent columns) holds all of its weight tile
   if (batch <= 16) return run<16, 128, 64, 2, WLayout::KN, Epi::ABSORB>(a, d.n_heads, 1, s);
   if (batch <= 32) return run<32, 128, 64, 2, WLayout::KN, Epi::ABSORB>(a, d.n_heads, 1, s);
@@ -388,7 +370,7 @@ cudaError_t launch_append(const mla_dims& d, int n_tokens, int d_model, const vo
   a.pos = pos;
   a.d_rope = d.d_rope;
   a.d_latent = d.d_latent;
-  a.rope_base = d.rope_base;
+  rope_turns_host(d.rope_base, d.d_rope, &a.rope);
   a.seq_idx = seq_idx;
   a.n_seqs = n_seqs;
   a.block_table = block_table;

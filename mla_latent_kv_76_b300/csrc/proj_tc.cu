@@ -33,7 +33,7 @@ struct ProjParams {
   // absorb only
   const __nv_bfloat16* q_r;
   const int32_t* pos;
-  float rope_base;
+  RopeTurns rope;
 };
 
 MLA_DEVI bool wait_done(uint64_t* b, uint32_t parity) {
@@ -43,39 +43,22 @@ MLA_DEVI bool wait_done(uint64_t* b, uint32_t parity) {
   return true;
 }
 
-// The RoPE frequencies base^(-2i/64) in fp64 for i < 32, one pow per CTA.
-MLA_DEVI void rope_thetas(double* theta, float base, int tid) {
-  __shared__ double s_r;
-  if (tid == 0) s_r = pow((double)base, -2.0 / 64.0);
-  __syncthreads();
-  if (tid < 32) {
-    double t = 1.0, r = s_r;
-    for (int e = tid; e; e >>= 1) {
-      if (e & 1) t *= r;
-      r *= r;
-    }
-    theta[tid] = t;
-  }
-  __syncthreads();
-}
-
 // ---------------------------------------------------------------- absorb
 // smem: q^C boxes [2][rows8 x 128 B] at 0, then W^UK boxes [8][128 k x 128 B].
 __global__ void __launch_bounds__(kThreads, 1)
     absorb_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                     const ProjParams p, int rows8, int32_t* status) {
+                     const __grid_constant__ ProjParams p, int rows8, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ double theta[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x;
   const int xbytes = rows8 * 128;
   uint8_t* sx = sm;
   uint8_t* sw = sm + ((2 * xbytes + 1023) & ~1023);
   if (tid == 0) {
-    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[0], 10);  // one arrival per issuing lane
     tc::mbar_init(&bars[1], 1);
     tc::fence_mbar_init();
   }
@@ -84,14 +67,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
-  if (tid == 0) {
-    tc::prefetch_map(&map_w);
-    tc::prefetch_map(&map_x);
-    tc::mbar_expect_tx(&bars[0], 8 * kBox + 2 * xbytes);
-    for (int j = 0; j < 8; ++j) tc::tma_load_3d(sw + j * kBox, &map_w, 64 * j, 0, h, &bars[0]);
-    for (int j = 0; j < 2; ++j) tc::tma_load_3d(sx + j * xbytes, &map_x, 64 * j, h, 0, &bars[0]);
+  // one box per issuing lane: a thread keeps only one or two copies moving at a time
+  if (tid < 8) {
+    tc::mbar_expect_tx(&bars[0], kBox);
+    tc::tma_load_3d(sw + tid * kBox, &map_w, 64 * tid, 0, h, &bars[0]);
+  } else if (tid < 10) {
+    tc::mbar_expect_tx(&bars[0], xbytes);
+    tc::tma_load_3d(sx + (tid - 8) * xbytes, &map_x, 64 * (tid - 8), h, 0, &bars[0]);
   }
-  rope_thetas(theta, p.rope_base, tid);
   bool ok = true;
   if (tid == 0) {
     ok = wait_done(&bars[0], 0);
@@ -139,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const __nv_bfloat16* src = p.q_r + ((int64_t)bb * p.n_heads + h) * 64 + 2 * i;
     const float x0 = __bfloat162float(src[0]), x1 = __bfloat162float(src[1]);
     float c, sn;
-    rope_cos_sin_theta(p.pos[bb], theta[i], &c, &sn);
+    rope_cos_sin(p.pos[bb], p.rope.hi[i], p.rope.lo[i], &c, &sn);
     __nv_bfloat16* dst = p.out + (int64_t)bb * p.out_sb + (int64_t)h * p.out_sh + 512 + 2 * i;
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x0 * c - x1 * sn, x0 * sn + x1 * c);
   }
@@ -155,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // smem: z boxes [8][rows8 x 128 B] at 0, then W^UV boxes [8][128 v x 128 B].
 __global__ void __launch_bounds__(kThreads, 1)
     out_proj_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                       const ProjParams p, int rows8, int32_t* status) {
+                       const __grid_constant__ ProjParams p, int rows8, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bars[2];
@@ -166,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sx = sm;
   uint8_t* sw = sm + ((8 * xbytes + 1023) & ~1023);
   if (tid == 0) {
-    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[0], 16);  // one arrival per issuing lane
     tc::mbar_init(&bars[1], 1);
     tc::fence_mbar_init();
   }
@@ -175,12 +158,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
+  if (tid < 8) {
+    tc::mbar_expect_tx(&bars[0], kBox);
+    tc::tma_load_3d(sw + tid * kBox, &map_w, 64 * tid, 0, h, &bars[0]);
+  } else if (tid < 16) {
+    tc::mbar_expect_tx(&bars[0], xbytes);
+    tc::tma_load_3d(sx + (tid - 8) * xbytes, &map_x, 64 * (tid - 8), h, 0, &bars[0]);
+  }
   if (tid == 0) {
-    tc::prefetch_map(&map_w);
-    tc::prefetch_map(&map_x);
-    tc::mbar_expect_tx(&bars[0], 8 * kBox + 8 * xbytes);
-    for (int j = 0; j < 8; ++j) tc::tma_load_3d(sw + j * kBox, &map_w, 64 * j, 0, h, &bars[0]);
-    for (int j = 0; j < 8; ++j) tc::tma_load_3d(sx + j * xbytes, &map_x, 64 * j, h, 0, &bars[0]);
     bool ok = wait_done(&bars[0], 0);
     if (ok) {
       tc::tc_fence_after();
@@ -253,18 +238,17 @@ struct AppendParams {
   int max_blocks, num_blocks, block_tokens;
   int64_t seq_stride;
   __nv_bfloat16* pool;
-  float rope_base;
+  RopeTurns rope;
   int32_t* status;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
     append_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
-                     const AppendParams p, int rows8) {
+                     const __grid_constant__ AppendParams p, int rows8) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ double theta[32];
   __shared__ float red[kAppendN * 32];  // this CTA's partial tile, [column][token t < 32]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = tc::cluster_rank();
@@ -276,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sh = sm;                                                    // [7][rows8 x 128 B]
   uint8_t* sw = sm + ((kAppendKBoxes * hbytes + 1023) & ~1023);        // [7][96 x 128 B]
   if (tid == 0) {
-    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[0], 2 * kAppendKBoxes);  // one arrival per issuing lane
     tc::mbar_init(&bars[1], 1);
     tc::fence_mbar_init();
   }
@@ -285,14 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
+  if (tid < kAppendKBoxes) {
+    tc::mbar_expect_tx(&bars[0], wbytes);
+    tc::tma_load_2d(sw + tid * wbytes, &map_w, k0 + 64 * tid, n0, &bars[0]);
+  } else if (tid < 2 * kAppendKBoxes) {
+    const int j = tid - kAppendKBoxes;
+    tc::mbar_expect_tx(&bars[0], hbytes);
+    tc::tma_load_2d(sh + j * hbytes, &map_h, k0 + 64 * j, 0, &bars[0]);
+  }
   if (tid == 0) {
-    tc::prefetch_map(&map_w);
-    tc::prefetch_map(&map_h);
-    tc::mbar_expect_tx(&bars[0], kAppendKBoxes * (wbytes + hbytes));
-    for (int j = 0; j < kAppendKBoxes; ++j) {
-      tc::tma_load_2d(sw + j * wbytes, &map_w, k0 + 64 * j, n0, &bars[0]);
-      tc::tma_load_2d(sh + j * hbytes, &map_h, k0 + 64 * j, 0, &bars[0]);
-    }
     bool ok = wait_done(&bars[0], 0);
     if (ok) {
       tc::tc_fence_after();
@@ -307,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) report(p.status, MLA_ERR_DEVICE_TIMEOUT);
   }
-  rope_thetas(theta, p.rope_base, tid);  // contains __syncthreads
+  __syncthreads();
   tc::tc_fence_after();
   __syncwarp();
   if (warp == 0) {  // token rows t < 32 live in TMEM lanes 0..31
@@ -359,7 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n >= 512) {
       float c, sn;
-      rope_cos_sin_theta(ps, theta[(n - 512) >> 1], &c, &sn);
+      const int i = (n - 512) >> 1;
+      rope_cos_sin(ps, p.rope.hi[i], p.rope.lo[i], &c, &sn);
       const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
       v0 = r0;
       v1 = r1;
@@ -486,7 +472,7 @@ cudaError_t launch_append_tc(const mla_dims& d, int n_tokens, int d_model, const
   p.block_tokens = d.block_tokens;
   p.seq_stride = seq_stride;
   p.pool = static_cast<__nv_bfloat16*>(pool);
-  p.rope_base = d.rope_base;
+  rope_turns_host(d.rope_base, 64, &p.rope);
   p.status = status;
   const int smem = append_smem_bytes(rows8);
   cudaLaunchConfig_t cfg = {};
@@ -528,7 +514,7 @@ cudaError_t launch_absorb_tc(const mla_dims& d, int batch, const void* q_c, cons
   p.out_sh = 576;
   p.q_r = static_cast<const __nv_bfloat16*>(q_r);
   p.pos = pos;
-  p.rope_base = d.rope_base;
+  rope_turns_host(d.rope_base, 64, &p.rope);
   const int smem = ((2 * rows8 * 128 + 1023) & ~1023) + 8 * kBox + 1024;
   cudaError_t e = ensure_smem<absorb_tc_kernel>(smem);
   if (e != cudaSuccess) return e;
