@@ -758,41 +758,72 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
   const int64_t Sb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   const int64_t T = red[1][0] + red[1][1] + red[1][2] + red[1][3];
   const int nb = tiles_of(effective_len(a.seqlens, b, cap, nullptr), kTile);
-  float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 32;
-  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 32;
+  // this block: latent columns [16 jg, 16 jg + 16) of every head of sequence b
+  float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 16;
+  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 16;
   if (nb == 0) {
-    for (int d = 0; d < 32; ++d) {
+    for (int d = 0; d < 16; ++d) {
       if (ZF32) zf[d] = 0.f; else zb[d] = __float2bfloat16_rn(0.f);
     }
     if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
     return;
   }
   const int g0 = worker_of(Sb, T, G), g1 = worker_of(Sb + nb - 1, T, G);
-  float M = -INFINITY;
-  for (int g = g0; g <= g1; ++g)
-    if (worker_begin(g + 1, T, G) > worker_begin(g, T, G)) M = fmaxf(M, m_part[((int64_t)g + b) * kH + h]);
-  float L = 0.f;
-  float4 acc[8];
+  // partials four at a time, all their loads in flight together; the running
+  // maximum M moves as chunks arrive (acc and L rescaled by 2^(M_old - M_new))
+  float M = -INFINITY, L = 0.f;
+  float4 acc[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int g = g0; g <= g1; ++g) {
-    if (worker_begin(g + 1, T, G) <= worker_begin(g, T, G)) continue;  // idle worker: no partial
-    const int64_t slot = (int64_t)g + b;
-    const float wgt = exp2f(m_part[slot * kH + h] - M);
-    L += wgt * l_part[slot * kH + h];
-    const float4* src = reinterpret_cast<const float4*>(a.o_part) + (slot * (kDC / 4) + jg * 8) * kH + h;
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g = g0; g <= g1; g += 4) {
+    float mv[4], lv[4];
+    float4 v[4][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 v = src[i * kH];
-      acc[i].x += wgt * v.x;
-      acc[i].y += wgt * v.y;
-      acc[i].z += wgt * v.z;
-      acc[i].w += wgt * v.w;
+    for (int u = 0; u < 4; ++u) {
+      const int gg = g + u;
+      // an idle worker (empty tile range) wrote no partial
+      const bool ok = gg <= g1 && worker_begin(gg + 1, T, G) > worker_begin(gg, T, G);
+      const int64_t slot = (int64_t)gg + b;
+      mv[u] = -INFINITY;
+      lv[u] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok) {
+        mv[u] = m_part[slot * kH + h];
+        lv[u] = l_part[slot * kH + h];
+        const float4* src = reinterpret_cast<const float4*>(a.o_part) + (slot * (kDC / 4) + jg * 4) * kH + h;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[u][i] = src[i * kH];
+      }
     }
+    const float Mn = fmaxf(M, fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])));
+    if (Mn == -INFINITY) continue;
+    const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+    L *= sc;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[i].x *= sc;
+      acc[i].y *= sc;
+      acc[i].z *= sc;
+      acc[i].w *= sc;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = (mv[u] == -INFINITY) ? 0.f : exp2f(mv[u] - Mn);
+      L += w * lv[u];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i].x += w * v[u][i].x;
+        acc[i].y += w * v[u][i].y;
+        acc[i].z += w * v[u][i].z;
+        acc[i].w += w * v[u][i].w;
+      }
+    }
+    M = Mn;
   }
   const float inv = 1.f / L;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const float4 v = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
     if (ZF32) {
       reinterpret_cast<float4*>(zf)[i] = v;
@@ -880,7 +911,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, map128, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid(kDC / 32, a.batch);
+  dim3 grid(kDC / 16, a.batch);
   if (a.z_is_fp32) combine_tc_kernel<true><<<grid, 128, 0, s>>>(a);
   else combine_tc_kernel<false><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();

@@ -75,6 +75,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_expect_tx(&bars[0], xbytes);
     tc::tma_load_3d(sx + (tid - 8) * xbytes, &map_x, 64 * (tid - 8), h, 0, &bars[0]);
   }
+  // ---- q^R part, RoPE(q^R, pos[b]) into columns [512, 576): independent of the
+  // MMA, so warps 1-3 do it while warp 0 waits for the weights (six rotations
+  // per thread per round, their loads issued together)
+  if (warp >= 1) {
+    constexpr int kU = 6;
+    const int n = p.batch * 32;
+    for (int base = tid - 32; base < n; base += 96 * kU) {
+      float x0[kU], x1[kU];
+      int ps[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * 96;
+        x0[u] = x1[u] = 0.f;
+        ps[u] = 0;
+        if (idx < n) {
+          const int bb = idx >> 5, i = idx & 31;
+          const __nv_bfloat16* src = p.q_r + ((int64_t)bb * p.n_heads + h) * 64 + 2 * i;
+          x0[u] = __bfloat162float(src[0]);
+          x1[u] = __bfloat162float(src[1]);
+          ps[u] = p.pos[bb];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * 96;
+        if (idx < n) {
+          const int bb = idx >> 5, i = idx & 31;
+          float c, sn;
+          rope_cos_sin(ps[u], p.rope.hi[i], p.rope.lo[i], &c, &sn);
+          __nv_bfloat16* dst = p.out + (int64_t)bb * p.out_sb + (int64_t)h * p.out_sh + 512 + 2 * i;
+          *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x0[u] * c - x1[u] * sn, x0[u] * sn + x1[u] * c);
+        }
+      }
+    }
+  }
   bool ok = true;
   if (tid == 0) {
     ok = wait_done(&bars[0], 0);
@@ -101,30 +136,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_t = tb + ((uint32_t)(warp * 32) << 16);
     __nv_bfloat16* dst = p.out + (int64_t)b * p.out_sb + (int64_t)h * p.out_sh;
 #pragma unroll 1
-    for (int c = 0; c < 16; ++c) {
-      uint32_t r[32];
-      tc::tmem_ld32(lane_t + c * 32, r);
+    for (int c = 0; c < 16; c += 2) {  // two loads per wait
+      uint32_t r[2][32];
+      tc::tmem_ld32(lane_t + c * 32, r[0]);
+      tc::tmem_ld32(lane_t + (c + 1) * 32, r[1]);
       tc::tmem_wait_ld();
       if (b < p.batch) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+        for (int k = 0; k < 2; ++k) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + (c + k) * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[k][8 * i]), __uint_as_float(r[k][8 * i + 1])),
+                               pack_bf16x2(__uint_as_float(r[k][8 * i + 2]), __uint_as_float(r[k][8 * i + 3])),
+                               pack_bf16x2(__uint_as_float(r[k][8 * i + 4]), __uint_as_float(r[k][8 * i + 5])),
+                               pack_bf16x2(__uint_as_float(r[k][8 * i + 6]), __uint_as_float(r[k][8 * i + 7])));
+        }
       }
     }
-  }
-  // ---- q^R part: RoPE(q^R, pos[b]) into columns [512, 576)
-  for (int idx = tid; idx < p.batch * 32; idx += kThreads) {
-    const int bb = idx >> 5, i = idx & 31;
-    const __nv_bfloat16* src = p.q_r + ((int64_t)bb * p.n_heads + h) * 64 + 2 * i;
-    const float x0 = __bfloat162float(src[0]), x1 = __bfloat162float(src[1]);
-    float c, sn;
-    rope_cos_sin(p.pos[bb], p.rope.hi[i], p.rope.lo[i], &c, &sn);
-    __nv_bfloat16* dst = p.out + (int64_t)bb * p.out_sb + (int64_t)h * p.out_sh + 512 + 2 * i;
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x0 * c - x1 * sn, x0 * sn + x1 * c);
   }
   tc::tc_fence_before();
   __syncthreads();
