@@ -27,9 +27,10 @@
 // Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns; lane c issues
 // column chunk c), warp 1 MMA,
 // warps 2-3 zero the rows past the sequence end in the last half tile (NaN
-// garbage must not meet a zero weight), warps 4-7 rescale O and write the
-// segment's partial (thread = head), warp 8 returns P buffers to the score CTA
-// once O has consumed them, warp 9 frees the score CTA's staging once P landed.
+// garbage must not meet a zero weight), warps 4-11 rescale O and write the
+// segment's partial (thread = head, two column halves).  The value MMA thread
+// frees the score CTA's staging once a P has landed, and its commit after the
+// MMAs that read a P buffer arrives on the score CTA's barrier for that buffer.
 //
 // Copies are issued from several lanes because one issuing thread keeps only
 // one or two bulk copies moving at a time (measured on B300: ~30 GB/s per
@@ -90,7 +91,7 @@ constexpr int kOffPrefix = kOffMisc + 32;
 constexpr int kBarCfull = 0, kBarCempty = 3, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
               kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35;
 // value CTA barriers
-constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOdone = 10, kBarOcomp = 14, kBarEvt = 15,
+constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOcomp = 14, kBarEvt = 15,
               kBarEvtdone = 16, kBarVcDrained = 17;
 
 // TMEM columns
@@ -100,7 +101,7 @@ constexpr uint32_t kColS = 0, kColQ = 256;
 
 enum { kEvtRescale = 1, kEvtEpilogue = 2, kEvtExit = 3 };
 
-size_t tc_smem_bytes(int batch) { return (size_t)kOffPrefix + (size_t)(batch + 1) * 4 + 1024; }
+size_t tc_smem_bytes(int batch) { return (size_t)kOffPrefix + 2 * (size_t)(batch + 1) * 4 + 1024; }
 
 struct TcParams {
   const __nv_bfloat16* q;
@@ -193,11 +194,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < kPBufs; ++i) {
         tc::mbar_init(&bars[kBarPfull + i], 1);  // the score CTA's expect_tx arrival + the copy
-        tc::mbar_init(&bars[kBarOdone + i], 1);
       }
       tc::mbar_init(&bars[kBarOcomp], 1);
       tc::mbar_init(&bars[kBarEvt], 1);
-      tc::mbar_init(&bars[kBarEvtdone], 128);
+      tc::mbar_init(&bars[kBarEvtdone], 256);
       tc::mbar_init(&bars[kBarVcDrained], 1);
     }
     *abort_flag = 0;
@@ -205,6 +205,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
   tile_prefix(p.seqlens, p.batch, cap, p.status, pre, kTile);  // ends with __syncthreads
+  int* Wp = pre + p.batch + 1;                                  // entries prefix of the split plan
+  plan_prefix(pre, p.batch, p.workers, Wp);                     // ends with __syncthreads
   tc::tc_fence_before();
   tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival
   tc::tc_fence_after();
@@ -212,8 +214,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const tc::Abort ab{abort_flag, p.status};
 
   const int B = p.batch, G = p.workers;
-  const int64_t T = pre[B];
-  const int64_t lo = worker_begin(g, T, G), hi = worker_begin(g + 1, T, G);
+  // worker g: entries [g E / G, (g + 1) E / G) of the plan, a contiguous run of tiles
+  const int64_t E = Wp[B];
+  const int64_t lo = entry_tile(pre, Wp, B, (int64_t)g * E / G), hi = entry_tile(pre, Wp, B, (int64_t)(g + 1) * E / G);
+  // the partial slot of a segment: the plan entry it starts with
+  auto slot_of = [&](const Seg& s) -> int64_t {
+    const int t = pre[s.b + 1] - pre[s.b], w = Wp[s.b + 1] - Wp[s.b];
+    return (int64_t)Wp[s.b] + entry_of_tile(s.t_begin, t, w);
+  };
 
   if (rank == 0) {
     // ================================================================ score CTA
@@ -234,6 +242,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int64_t x = lo; x < hi && ok;) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
           x += s.ntile;
+          // the next segment's query (147 KB) is warmed in L2 a whole segment ahead
+          if (c == 0 && x < hi)
+            tc::prefetch_l2(p.q + (int64_t)seq_of_tile(pre, B, x) * kH * kD, (uint32_t)(kH * kD * 2));
           for (int j = 0; j < s.ntile; ++j, ++m) {
             const int tt = s.t_begin + j;
             if (m >= 1 && !tc::wait<false>(&bars[kBarCempty + t], (m - 1) & 1, ab)) {
@@ -344,13 +355,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int pb = hidx % kPBufs, up = hidx / kPBufs;
               if (!tc::wait<false>(&bars[kBarStgFull + w], u & 1, ab)) { ok = false; break; }
               if (up >= 1 && !tc::wait<true>(&bars[kBarPfree + pb], (up - 1) & 1, ab)) { ok = false; break; }
-              // the value CTA's warp 9 frees the staging (kBarStgFree) once the copy landed
+              // the value CTA's MMA thread frees the staging (kBarStgFree) once the copy landed
               tc::bulk_copy_to_peer(r_p + pb * kPBufBytes, stg, kPBufBytes, r_pfull + pb * 8);
               ++u;
             }
             hh += nh;
           }
         }
+        // The value CTA's MMA commits arrive on kBarPfree asynchronously: before this
+        // CTA may exit, the last arrival on every P buffer must have landed.
+        if (w == 0 && ok)
+          for (int pb = 0; pb < kPBufs; ++pb) {
+            const int uses = (hh - pb + kPBufs - 1) / kPBufs;
+            if (uses >= 1) tc::wait<true>(&bars[kBarPfree + pb], (uses - 1) & 1, ab);
+          }
       }
     } else if (warp >= 4) {
       // ------------------------------------------------------------ softmax (thread = head)
@@ -365,25 +383,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto load_q = [&](int b) {
         const __nv_bfloat16* row = p.q + ((int64_t)b * kH + h) * kD;
         const uint4* src = reinterpret_cast<const uint4*>(row + 256 * w);  // latent [256 w, 256 w + 256)
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = __ldg(src + c * 8 + i);
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
-          }
-          tc::tmem_st32(lane_t + kColQ + 128 * w + c * 32, r);
-        }
         // RoPE columns [32 w, 32 w + 32) of the row: 16-byte pieces 4 w .. 4 w + 3 of a
-        // 128-byte-swizzled K-major row
+        // 128-byte-swizzled K-major row; loaded with the first half of the latent part
         const uint4* srcr = reinterpret_cast<const uint4*>(row + kDC);
+        uint4 rq[4];
 #pragma unroll
-        for (int c = 4 * w; c < 4 * w + 4; ++c)
-          *reinterpret_cast<uint4*>(sm + kOffQrope + h * 128 + ((c ^ (h & 7)) * 16)) = __ldg(srcr + c);
+        for (int c = 0; c < 4; ++c) rq[c] = __ldg(srcr + 4 * w + c);
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {  // 16 loads in flight per thread per round
+          uint32_t r[2][32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint4 v = __ldg(src + c2 * 16 + i);
+            r[i >> 3][4 * (i & 7)] = v.x;
+            r[i >> 3][4 * (i & 7) + 1] = v.y;
+            r[i >> 3][4 * (i & 7) + 2] = v.z;
+            r[i >> 3][4 * (i & 7) + 3] = v.w;
+          }
+          tc::tmem_st32(lane_t + kColQ + 128 * w + c2 * 64, r[0]);
+          tc::tmem_st32(lane_t + kColQ + 128 * w + c2 * 64 + 32, r[1]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(sm + kOffQrope + h * 128 + (((4 * w + c) ^ (h & 7)) * 16)) = rq[c];
         tc::fence_async_smem();
         tc::tmem_wait_st();
         tc::tc_fence_before();
@@ -478,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars[kBarLsum]);
         if (!tc::wait<false>(&bars[kBarLsum], k & 1, ab)) break;
         if (w == 0) {
-          const int64_t slot = (int64_t)g + s.b;
+          const int64_t slot = slot_of(s);
           p.m_part[slot * kH + h] = m_ref;
           p.l_part[slot * kH + h] = l + lsum[h];
         }
@@ -535,6 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // ---------------------------------------------------------- value MMA
         constexpr uint32_t idO = tc::idesc_bf16(128, 256, 0, 1);
+        const uint32_t r_stgfree = tc::map_peer(&bars[kBarStgFree], 0);
         const uint32_t stg0 = smem_u32(sm + kOffStage);
         const uint32_t pb0 = smem_u32(sm + kOffP);
         int hh = 0, oc = 0, ev = 0;
@@ -567,6 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ++ntail[st];
               }
               if (!tc::wait<false>(&bars[kBarPfull + pb], (hh / kPBufs) & 1, ab)) { ok = false; break; }
+              tc::mbar_arrive_cluster_addr(r_stgfree + w * 8);  // P landed: the score CTA may reuse its staging
               const volatile int* fl = reinterpret_cast<const volatile int*>(sm + kOffP + pb * kPBufBytes + kPMetaFlags);
               if (fl[0] | fl[1] | fl[2] | fl[3]) {  // the reference maximum moved: rescale O first
                 if (!drain() || !post(kEvtRescale, pb, 0)) { ok = false; break; }
@@ -581,13 +605,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              tc::smem_desc(sa + n2 * 4 * kChunkBytes + kk * 2048, kChunkBytes, 1024), idO,
                              (first_half && kk == 0) ? 0u : 1u);
               tc::mma_commit(&bars[kBarEmpty + st]);
-              tc::mma_commit(&bars[kBarOdone + pb]);
+              // P buffer pb is free once these MMAs are done: signal the score CTA's
+              // kBarPfree + pb directly (same offset in the peer, cluster rank 0)
+              tc::mma_commit_multicast(&bars[kBarPfree + pb], 1);
               first_half = false;
             }
           }
           if (!ok) break;
           // segment end: the partial's O goes out before the next segment overwrites it
-          if (!drain() || !post(kEvtEpilogue, 0, g + s.b)) break;
+          if (!drain() || !post(kEvtEpilogue, 0, (int)slot_of(s))) break;
         }
         post(kEvtExit, 0, 0);
         tc::mma_commit(&bars[kBarVcDrained]);
@@ -626,9 +652,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else if (warp < 8) {
+    } else if (warp >= 4) {
       // ------------------------------------------------------------ rescale / epilogue (thread = head)
-      const int h = tid - 128;
+      // warps 4-7 take accumulator columns [0, 256), warps 8-11 columns [256, 512)
+      const int h = (tid - 128) & 127;
+      const int c0 = warp >= 8 ? 8 : 0;  // first 32-column group of this warpgroup
       const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
       for (int e = 0;; ++e) {
         if (!tc::wait<false>(&bars[kBarEvt], e & 1, ab)) break;
@@ -638,13 +666,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (type == kEvtRescale) {
           const float a = reinterpret_cast<const float*>(sm + kOffP + arg * kPBufBytes + kPMetaAlpha)[h];
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            uint32_t r[32];
-            tc::tmem_ld32(lane_t + c * 32, r);
+          for (int c = c0; c < c0 + 8; c += 2) {
+            uint32_t r0[32], r1[32];
+            tc::tmem_ld32(lane_t + c * 32, r0);
+            tc::tmem_ld32(lane_t + c * 32 + 32, r1);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-            tc::tmem_st32(lane_t + c * 32, r);
+            for (int i = 0; i < 32; ++i) {
+              r0[i] = __float_as_uint(__uint_as_float(r0[i]) * a);
+              r1[i] = __float_as_uint(__uint_as_float(r1[i]) * a);
+            }
+            tc::tmem_st32(lane_t + c * 32, r0);
+            tc::tmem_st32(lane_t + c * 32 + 32, r1);
           }
           tc::tmem_wait_st();
         } else {
@@ -652,7 +685,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // 32 lanes of a warp store 512 contiguous bytes
           float4* dst = reinterpret_cast<float4*>(p.o_part) + (int64_t)slot * (kDC / 4) * kH + h;
 #pragma unroll 1
-          for (int c = 0; c < 16; c += 2) {
+          for (int c = c0; c < c0 + 8; c += 2) {
             uint32_t r0[32], r1[32];
             tc::tmem_ld32(lane_t + c * 32, r0);
             tc::tmem_ld32(lane_t + c * 32 + 32, r1);
@@ -668,49 +701,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_before();
         tc::mbar_arrive(&bars[kBarEvtdone]);
-      }
-    } else if (warp == 9) {
-      if (lane == 0) {
-        // ---------------------------------------------------------- P landed: the score CTA may reuse its staging
-        const uint32_t r_stgfree = tc::map_peer(&bars[kBarStgFree], 0);
-        int hh = 0;
-        bool ok = true;
-        for (int64_t x = lo; x < hi && ok;) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
-          x += s.ntile;
-          for (int j = 0; j < s.ntile && ok; ++j) {
-            const int nh = halves_of(s, s.t_begin + j);
-            for (int w = 0; w < nh; ++w, ++hh) {
-              if (!tc::wait<false>(&bars[kBarPfull + hh % kPBufs], (hh / kPBufs) & 1, ab)) {
-                ok = false;
-                break;
-              }
-              tc::mbar_arrive_cluster_addr(r_stgfree + w * 8);
-            }
-          }
-        }
-      }
-    } else if (warp == 8) {
-      if (lane == 0) {
-        // ---------------------------------------------------------- P buffers back to the score CTA
-        const uint32_t r_pfree = tc::map_peer(sm + kOffBar + kBarPfree * 8, 0);
-        int hh = 0;
-        bool ok = true;
-        for (int64_t x = lo; x < hi && ok;) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
-          x += s.ntile;
-          for (int j = 0; j < s.ntile && ok; ++j) {
-            const int nh = halves_of(s, s.t_begin + j);
-            for (int w = 0; w < nh; ++w, ++hh) {
-              const int pb = hh % kPBufs;
-              if (!tc::wait<false>(&bars[kBarOdone + pb], (hh / kPBufs) & 1, ab)) {
-                ok = false;
-                break;
-              }
-              tc::mbar_arrive_cluster_addr(r_pfree + pb * 8);
-            }
-          }
-        }
       }
     }
   }
@@ -729,7 +719,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Partials are unnormalised: O_s with reference maximum m_s (log2 units) and
 // weight sum l_s.  M = max_s m_s, L = sum_s l_s 2^(m_s - M),
 // z = sum_s 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.
-// Block (column group of 32, sequence b), thread = head: the partial reads are
+// Block (column group of 16, sequence b), thread = head: the partial reads are
 // 512 contiguous bytes per warp.
 template <bool ZF32>
 __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
@@ -738,25 +728,42 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
   const float* m_part = a.lse_part;
   const float* l_part = a.l_part;
   const int64_t cap = a.block_table ? (int64_t)a.max_blocks * 64 : a.seq_stride;
-  long long before = 0, total = 0;
+  // the split plan of the partial kernel: total tiles T, non-empty sequences n,
+  // then the entries of the sequences before b (W_b) and of b itself
+  __shared__ long long red[2][4];
+  __shared__ long long s_tot[2];
+  long long total = 0, nonempty = 0;
   for (int i = h; i < a.batch; i += blockDim.x) {
     const int t = tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile);
     total += t;
-    if (i < b) before += t;
+    nonempty += t > 0;
   }
-  __shared__ long long red[2][4];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
     total += __shfl_xor_sync(0xffffffffu, total, o);
+    nonempty += __shfl_xor_sync(0xffffffffu, nonempty, o);
   }
   if (lane == 0) {
-    red[0][warp] = before;
-    red[1][warp] = total;
+    red[0][warp] = total;
+    red[1][warp] = nonempty;
   }
   __syncthreads();
-  const int64_t Sb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-  const int64_t T = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  if (h == 0) {
+    s_tot[0] = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+    s_tot[1] = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  }
+  __syncthreads();
+  const int64_t T = s_tot[0];
+  const int n_ne = (int)s_tot[1];
+  long long before = 0;
+  for (int i = h; i < b; i += blockDim.x)
+    before += plan_entries(tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile), T, n_ne, G);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  __syncthreads();  // red[] is reused
+  if (lane == 0) red[0][warp] = before;
+  __syncthreads();
+  const int64_t Wb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   const int nb = tiles_of(effective_len(a.seqlens, b, cap, nullptr), kTile);
   // this block: latent columns [16 jg, 16 jg + 16) of every head of sequence b
   float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 16;
@@ -768,22 +775,21 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
     if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
     return;
   }
-  const int g0 = worker_of(Sb, T, G), g1 = worker_of(Sb + nb - 1, T, G);
+  // sequence b's partials are slots [Wb, Wb + wb), every one of them written
+  const int64_t g0 = Wb, g1 = Wb + plan_entries(nb, T, n_ne, G) - 1;
   // partials four at a time, all their loads in flight together; the running
   // maximum M moves as chunks arrive (acc and L rescaled by 2^(M_old - M_new))
   float M = -INFINITY, L = 0.f;
   float4 acc[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int g = g0; g <= g1; g += 4) {
+  for (int64_t g = g0; g <= g1; g += 4) {
     float mv[4], lv[4];
     float4 v[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int gg = g + u;
-      // an idle worker (empty tile range) wrote no partial
-      const bool ok = gg <= g1 && worker_begin(gg + 1, T, G) > worker_begin(gg, T, G);
-      const int64_t slot = (int64_t)gg + b;
+      const int64_t slot = g + u;
+      const bool ok = slot <= g1;
       mv[u] = -INFINITY;
       lv[u] = 0.f;
 #pragma unroll

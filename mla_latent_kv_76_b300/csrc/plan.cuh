@@ -79,4 +79,78 @@ MLA_DEVI int seq_of_tile(const int* pre, int B, int64_t x) {
   return lo;
 }
 
+// ---------------------------------------------------------------- sequence-aligned plan
+// (tensor-core decode) Sequence b with t_b > 0 tiles is cut into w_b entries,
+//   w_b = min(t_b, 1 + floor((G - n) t_b / T))    (w_b = 1 when G <= n),
+// n = number of non-empty sequences, T = total tiles, G = workers.  Entry k of
+// b covers tiles [floor(t_b k / w_b), floor(t_b (k+1) / w_b)) (never empty, as
+// w_b <= t_b), and the entries total at most max(G, n).  Worker g takes
+// entries [floor(g E / G), floor((g+1) E / G)), so a worker never straddles
+// two sequences when E <= G (each one writes a single partial, with no second
+// epilogue or query reload), and otherwise takes whole sequences.  Entry e's
+// partial lives in slot e.
+MLA_DEVI int plan_entries(int t, int64_t T, int n, int G) {
+  if (t <= 0) return 0;
+  if (G <= n) return 1;
+  const int64_t w = 1 + (int64_t)(G - n) * t / T;
+  return (int)(w < t ? w : t);
+}
+MLA_DEVI int entry_start(int k, int t, int w) { return (int)((int64_t)t * k / w); }
+// The entry (index within its sequence) holding tile tau of a sequence of t tiles.
+MLA_DEVI int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau + 1) * w - 1) / t); }
+
+// Exclusive prefix of plan_entries over b into W[0..B] (shared memory), from the
+// tile prefix pre[0..B]; every thread of the block takes part.
+MLA_DEVI void plan_prefix(const int* pre, int B, int G, int* W) {
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (B + nthr - 1) / nthr;
+  const int b0 = tid * per, b1 = min(B, b0 + per);
+  __shared__ int red[32];
+  __shared__ int s_n;
+  int n = 0;
+  for (int b = b0; b < b1; ++b) n += pre[b + 1] > pre[b];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if (lane == 0) red[warp] = n;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+    for (int w = 0; w < (nthr + 31) / 32; ++w) t += red[w];
+    s_n = t;
+  }
+  __syncthreads();
+  const int64_t T = pre[B];
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += plan_entries(pre[b + 1] - pre[b], T, s_n, G);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  __syncthreads();  // red[] is reused
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  int warp_off = 0;
+  for (int w = 0; w < warp; ++w) warp_off += red[w];
+  int run = warp_off + incl - local;
+  for (int b = b0; b < b1; ++b) {
+    W[b] = run;
+    run += plan_entries(pre[b + 1] - pre[b], T, s_n, G);
+  }
+  if (tid == nthr - 1) W[B] = run;
+  __syncthreads();
+}
+
+// The sequence owning entry e < W[B]: the largest b with W[b] <= e.
+MLA_DEVI int seq_of_entry(const int* W, int B, int64_t e) { return seq_of_tile(W, B, e); }
+
+// First global tile of entry e (T for e == E).
+MLA_DEVI int64_t entry_tile(const int* pre, const int* W, int B, int64_t e) {
+  if (e >= W[B]) return pre[B];
+  const int b = seq_of_entry(W, B, e);
+  const int t = pre[b + 1] - pre[b], w = W[b + 1] - W[b];
+  return pre[b] + entry_start((int)(e - W[b]), t, w);
+}
+
 }  // namespace mla

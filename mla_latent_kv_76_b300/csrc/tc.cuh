@@ -197,6 +197,14 @@ MLA_DEVI void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+// Commit to the mbarrier at the same shared-memory offset as `bar` in every CTA
+// of the cluster named in cta_mask (bit r = cluster rank r).
+MLA_DEVI void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(cta_mask)
+               : "memory");
+}
 
 // ---------------------------------------------------------------- cluster
 MLA_DEVI uint32_t cluster_rank() {
