@@ -89,7 +89,8 @@ constexpr int kOffPrefix = kOffMisc + 32;
 
 // score CTA barriers
 constexpr int kBarCfull = 0, kBarCempty = 3, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
-              kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35;
+              kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35,
+              kBarQringFree = 37;
 // value CTA barriers
 constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOcomp = 14, kBarEvt = 15,
               kBarEvtdone = 16, kBarVcDrained = 17;
@@ -154,7 +155,7 @@ MLA_DEVI int half_block(const TcParams& p, const Seg& s, int tt, int w) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map, const __grid_constant__ CUtensorMap cache_map128,
-                     const TcParams p) {
+                     const __grid_constant__ CUtensorMap q_map, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -186,6 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[kBarXmax], 256);
       tc::mbar_init(&bars[kBarXmax + 1], 256);
       tc::mbar_init(&bars[kBarLsum], 256);
+      tc::mbar_init(&bars[kBarQringFree], 256);
     } else {
       for (int i = 0; i < kVStages; ++i) {
         tc::mbar_init(&bars[kBarFull + i], 8);  // one arrival per issuing lane
@@ -239,6 +241,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint64_t* fb = &bars[kBarCfull + t];
         bool ok = true;
         int m = 0;  // tiles loaded so far
+        // The first segment's query (128 heads x 576 = exactly the three ring
+        // slots, same 128-byte-swizzled layout) comes through the ring ahead of
+        // tile 0: as per-thread loads it took ~7 us to arrive and held back the
+        // tile copies.  The softmax warps move it to TMEM and free the ring.
+        if (lo < hi) {
+          tc::prefetch_map(&q_map);
+          tc::mbar_expect_tx(fb, kChunk128);
+          tc::tma_load_3d(dst, &q_map, c * 64, 0, seq_of_tile(pre, B, lo), fb);
+          ok = tc::wait<false>(&bars[kBarQringFree], 0, ab);
+        }
         for (int64_t x = lo; x < hi && ok;) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
           x += s.ntile;
@@ -282,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (m >= 1) tc::wait<false>(fb, (m - 1) & 1, ab);  // no copy in flight at exit
+        if (lo < hi) tc::wait<false>(fb, m & 1, ab);  // no copy in flight at exit (fills: the query + m tiles)
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -307,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // straight-line issue: per ring slot (three chunks) one wait, twelve MMAs, one commit
 #pragma unroll
             for (int t = 0; t < kSlots; ++t) {
-              if (!tc::wait<false>(&bars[kBarCfull + t], m & 1, ab)) {
+              if (!tc::wait<false>(&bars[kBarCfull + t], (m + 1) & 1, ab)) {  // phase 0 held the query
                 ok = false;
                 break;
               }
@@ -412,12 +424,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars[kBarQready]);
       };
 
+      // the first segment's query, TMA-loaded into the three ring slots: latent
+      // chunks 4 w .. 4 w + 3 of row h to TMEM, the RoPE chunk (8) to kOffQrope
+      // (same swizzled layout, so a straight copy), then the ring goes back to the
+      // producer
+      auto q_from_ring = [&]() -> bool {
+        for (int t = 0; t < kSlots; ++t)
+          if (!tc::wait<false>(&bars[kBarCfull + t], 0, ab)) return false;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = 4 * w + cc;
+          const uint8_t* row = sm + kOffRing + (c / 3) * kSlotBytes + (c % 3) * kChunk128 + h * 128;
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((j ^ (h & 7)) * 16));
+            r[4 * j] = v.x;
+            r[4 * j + 1] = v.y;
+            r[4 * j + 2] = v.z;
+            r[4 * j + 3] = v.w;
+          }
+          tc::tmem_st32(lane_t + kColQ + 128 * w + 32 * cc, r);
+        }
+        const uint8_t* rope = sm + kOffRing + 2 * kSlotBytes + 2 * kChunk128 + h * 128 + 64 * w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(sm + kOffQrope + h * 128 + 64 * w + 16 * j) =
+              *reinterpret_cast<const uint4*>(rope + 16 * j);
+        tc::fence_async_smem();
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[kBarQready]);
+        tc::mbar_arrive(&bars[kBarQringFree]);
+        return true;
+      };
+
       int m = 0, hh = 0, k = 0;
       bool ok = true, first = true;
       for (int64_t x = lo; x < hi && ok; ++k) {
         const Seg s = seg_at(pre, B, x, hi, p, cap);
         x += s.ntile;
-        if (first) load_q(s.b);
+        if (first) {
+          if (!q_from_ring()) break;
+        }
         first = false;
         float m_ref = -INFINITY, l = 0.f;
         for (int j = 0; j < s.ntile; ++j, ++m) {
@@ -886,6 +935,17 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // the query [B][128][576] for the score CTA's first segment, one box per 64 columns
+  CUtensorMap qmap;
+  {
+    const cuuint64_t qdims[3] = {(cuuint64_t)kD, (cuuint64_t)kH, (cuuint64_t)a.batch};
+    const cuuint64_t qstrides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kH * kD * 2};
+    const cuuint32_t qbox[3] = {64, 128, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qdims, qstrides, qbox, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   // the score CTA's whole-tile boxes (contiguous cache only)
   CUtensorMap map128 = map;
   if (!a.block_table) {
@@ -914,7 +974,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(a.batch);
   cudaError_t e = ensure_smem<decode_tc_kernel>((int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, map128, p);
+  decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, map128, qmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 grid(kDC / 16, a.batch);
