@@ -125,7 +125,8 @@ enum {
  *   s_j   = scale * (q[b][i][0:d_c] . c_j + q[b][i][d_c:] . k^R_j)
  *   lse   = log sum_j exp(s_j)
  *   z     = sum_j exp(s_j - lse) c_j
- * computed as split-KV partial passes (online softmax over 64-token tiles)
+ * computed as split-KV partial passes (online softmax over 64-token tiles, or
+ * 128-token tiles on the tensor-core path for n_h = 128, d_c = 512, d_R = 64)
  * followed by a log-sum-exp combine.  A sequence with seqlens[b] == 0 gives
  * z = 0, lse = -inf.
  *   q        [batch][n_h][d_c + d_R] bf16 (output of mla_absorb_q)
@@ -133,8 +134,13 @@ enum {
  *            cache layout as above (read only)
  *   seqlens  [batch] int32 device array
  *   scale    softmax scale, normally 1/sqrt(d_h + d_R)
- *   num_workers  split-KV workers (0 = automatic); the result is the same
- *            for every value up to floating-point rounding
+ *   num_workers  split-KV workers (0 = automatic: one per SM pair on the
+ *            tensor-core path); the result is the same for every value up to
+ *            floating-point rounding.  The tensor-core path cuts sequence b
+ *            into w_b = min(t_b, 1 + floor((G - n) t_b / T)) pieces (t_b its
+ *            128-token tiles, T their sum, n non-empty sequences, G workers;
+ *            one piece per sequence when G <= n), so no worker spans two
+ *            sequences while the pieces fit the workers.
  *   workspace / workspace_bytes: device scratch of at least
  *            mla_decode_workspace_size(dims, batch, num_workers) bytes; its
  *            contents on entry do not matter
