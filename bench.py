@@ -47,7 +47,7 @@ def workload_desc(wl):
                     f"append 1 token/seq (d=7168)",
         "batch": wl.batch, "seqlen": int(wl.seqlens[0]), "n_heads": wl.n_heads, "d_latent": wl.d_latent,
         "d_rope": wl.d_rope, "d_head": wl.d_head, "d_model": wl.d_model,
-        "step": "absorb_q + append_cache + decode_attn(partial+combine) + out_proj",
+        "step": "absorb_q || append_cache (two streams), then decode_attn (partial+combine), then out_proj",
         "l2": f"inputs larger than L2: {ROTATE} rotating copies of the layer state (cache + weights)",
     }
 
@@ -185,12 +185,21 @@ def run_ours(args, rank, world, local_rank):
     o = torch.empty((B, wl.n_heads, wl.d_v), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
 
     def step(i):
+        # absorb and append touch disjoint data, so they run on two streams
+        # (fork / join); decode needs both, out_proj needs decode
         L = layers[i % ROTATE]
+        fork.record(stream)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            mla.mla_append_cache(dims, h, L["w_kv"], app_seq, app_pos, L["pool"], n_seqs=B,
+                                 seq_stride=wl.seq_stride, dev_status=status)
+            join.record(side)
         mla.mla_absorb_q(dims, q_c, q_r, q_pos, L["w_uk"], q_out=q)
-        mla.mla_append_cache(dims, h, L["w_kv"], app_seq, app_pos, L["pool"], n_seqs=B,
-                             seq_stride=wl.seq_stride, dev_status=status)
+        stream.wait_event(join)
         decode(i)
         mla.mla_out_proj(dims, z, L["w_uv"], o_out=o)
 
