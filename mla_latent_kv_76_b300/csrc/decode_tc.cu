@@ -639,7 +639,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ++ntail[st];
               }
               if (!tc::wait<false>(&bars[kBarPfull + pb], (hh / kPBufs) & 1, ab)) { ok = false; break; }
-              tc::mbar_arrive_cluster_addr(r_stgfree + w * 8);  // P landed: the score CTA may reuse its staging
+              // P landed (the copy's bytes completed the barrier just observed), so the
+              // score CTA may reuse its staging; this arrive orders nothing of this thread's
+              tc::mbar_arrive_cluster_addr_relaxed(r_stgfree + w * 8);
               const volatile int* fl = reinterpret_cast<const volatile int*>(sm + kOffP + pb * kPBufBytes + kPMetaFlags);
               if (fl[0] | fl[1] | fl[2] | fl[3]) {  // the reference maximum moved: rescale O first
                 if (!drain() || !post(kEvtRescale, pb, 0)) { ok = false; break; }

@@ -241,6 +241,11 @@ MLA_DEVI void st_cluster_u32(uint32_t addr, uint32_t a) {
 MLA_DEVI void mbar_arrive_cluster_addr(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
+// Same without release semantics: for a signal that orders none of this thread's
+// own memory operations (a cluster-scope release can stall the thread).
+MLA_DEVI void mbar_arrive_cluster_addr_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
 // Copy `bytes` (a multiple of 16) from this CTA's shared memory to another
 // CTA of the cluster (shared::cluster address `dst`) with the bulk-copy
 // engine.  Arrives on the destination's barrier with the byte count as
