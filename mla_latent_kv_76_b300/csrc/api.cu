@@ -187,6 +187,7 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.scale = scale;
   a.workers = G;
   a.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_o);
+  a.plan_flag = static_cast<int32_t*>(workspace);  // first word of the 256-byte header
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse);
   a.l_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_l);
   a.z_out = z_out;

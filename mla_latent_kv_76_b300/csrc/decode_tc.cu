@@ -120,6 +120,7 @@ struct TcParams {
   float* m_part;    // [(G + B)][128]       reference maximum, log2 units
   float* l_part;    // [(G + B)][128]       sum of weights relative to m_part
   int32_t* status;
+  int32_t* plan_flag;  // 1: sequence-aligned plan, 0: even tile split (read by the combine)
 };
 
 struct Seg {
@@ -209,6 +210,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tile_prefix(p.seqlens, p.batch, cap, p.status, pre, kTile);  // ends with __syncthreads
   int* Wp = pre + p.batch + 1;                                  // entries prefix of the split plan
   plan_prefix(pre, p.batch, p.workers, Wp);                     // ends with __syncthreads
+  const bool aligned = prefer_aligned_plan(pre, Wp, p.batch, p.workers);
+  if (blockIdx.x == 0 && tid == 0) *p.plan_flag = aligned ? 1 : 0;
   tc::tc_fence_before();
   tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival
   tc::tc_fence_after();
@@ -216,11 +219,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const tc::Abort ab{abort_flag, p.status};
 
   const int B = p.batch, G = p.workers;
-  // worker g: entries [g E / G, (g + 1) E / G) of the plan, a contiguous run of tiles
-  const int64_t E = Wp[B];
-  const int64_t lo = entry_tile(pre, Wp, B, (int64_t)g * E / G), hi = entry_tile(pre, Wp, B, (int64_t)(g + 1) * E / G);
-  // the partial slot of a segment: the plan entry it starts with
+  // worker g's contiguous run of tiles: entries [g E / G, (g + 1) E / G) of the
+  // sequence-aligned plan, or the even split [g T / G, (g + 1) T / G)
+  const int64_t E = Wp[B], T = pre[B];
+  const int64_t lo = aligned ? entry_tile(pre, Wp, B, (int64_t)g * E / G) : worker_begin(g, T, G);
+  const int64_t hi = aligned ? entry_tile(pre, Wp, B, (int64_t)(g + 1) * E / G) : worker_begin(g + 1, T, G);
+  // the partial slot of a segment: the plan entry it starts with, or worker + sequence
   auto slot_of = [&](const Seg& s) -> int64_t {
+    if (!aligned) return (int64_t)g + s.b;
     const int t = pre[s.b + 1] - pre[s.b], w = Wp[s.b + 1] - Wp[s.b];
     return (int64_t)Wp[s.b] + entry_of_tile(s.t_begin, t, w);
   };
@@ -806,15 +812,26 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
   __syncthreads();
   const int64_t T = s_tot[0];
   const int n_ne = (int)s_tot[1];
-  long long before = 0;
-  for (int i = h; i < b; i += blockDim.x)
-    before += plan_entries(tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile), T, n_ne, G);
+  long long before = 0, tiles_before = 0;
+  for (int i = h; i < b; i += blockDim.x) {
+    const int t = tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile);
+    before += plan_entries(t, T, n_ne, G);
+    tiles_before += t;
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    tiles_before += __shfl_xor_sync(0xffffffffu, tiles_before, o);
+  }
   __syncthreads();  // red[] is reused
-  if (lane == 0) red[0][warp] = before;
+  if (lane == 0) {
+    red[0][warp] = before;
+    red[1][warp] = tiles_before;
+  }
   __syncthreads();
   const int64_t Wb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+  const int64_t Sb = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  const bool aligned = *a.plan_flag != 0;
   const int nb = tiles_of(effective_len(a.seqlens, b, cap, nullptr), kTile);
   // this block: latent columns [16 jg, 16 jg + 16) of every head of sequence b
   float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 16;
@@ -826,8 +843,11 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
     if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
     return;
   }
-  // sequence b's partials are slots [Wb, Wb + wb), every one of them written
-  const int64_t g0 = Wb, g1 = Wb + plan_entries(nb, T, n_ne, G) - 1;
+  // sequence b's partials: slots [Wb, Wb + wb) (aligned plan, every one written),
+  // or slot g + b of each worker g whose tiles touch b (even split; a worker with
+  // no tiles wrote nothing)
+  const int64_t g0 = aligned ? Wb : worker_of(Sb, T, G);
+  const int64_t g1 = aligned ? Wb + plan_entries(nb, T, n_ne, G) - 1 : worker_of(Sb + nb - 1, T, G);
   // partials four at a time, all their loads in flight together; the running
   // maximum M moves as chunks arrive (acc and L rescaled by 2^(M_old - M_new))
   float M = -INFINITY, L = 0.f;
@@ -839,8 +859,9 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
     float4 v[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int64_t slot = g + u;
-      const bool ok = slot <= g1;
+      const int64_t gg = g + u;
+      const int64_t slot = aligned ? gg : gg + b;
+      const bool ok = gg <= g1 && (aligned || worker_begin((int)gg + 1, T, G) > worker_begin((int)gg, T, G));
       mv[u] = -INFINITY;
       lv[u] = 0.f;
 #pragma unroll
@@ -973,6 +994,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   p.m_part = a.lse_part;
   p.l_part = a.l_part;
   p.status = a.status;
+  p.plan_flag = a.plan_flag;
   const size_t smem = tc_smem_bytes(a.batch);
   cudaError_t e = ensure_smem<decode_tc_kernel>((int)smem);
   if (e != cudaSuccess) return e;

@@ -153,4 +153,52 @@ MLA_DEVI int64_t entry_tile(const int* pre, const int* W, int B, int64_t e) {
   return pre[b] + entry_start((int)(e - W[b]), t, w);
 }
 
+// Which plan a tensor-core decode call uses.  The sequence-aligned plan costs its
+// longest entry (tiles); the even split of the tile list costs its most
+// expensive worker, tiles + kSegPenaltyTiles per sequence beyond the first (each
+// extra sequence costs one more partial write and a query reload, ~3 tiles of
+// time).  The aligned plan wins on uniform batches (16 x 4096: 8 vs 10); the
+// even split wins when sequences outnumber half the workers and their lengths
+// vary (64 sequences of 1024..8192 tokens: 64 vs 40).  Every thread of the block
+// gets the same answer.
+constexpr int kSegPenaltyTiles = 3;
+MLA_DEVI bool prefer_aligned_plan(const int* pre, const int* W, int B, int G) {
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t T = pre[B];
+  int64_t ca = 0, cb = 0;
+  for (int b = tid; b < B; b += nthr) {
+    const int t = pre[b + 1] - pre[b], w = W[b + 1] - W[b];
+    if (t > 0 && w > 0) ca = max(ca, (int64_t)((t + w - 1) / w));
+  }
+  for (int g = tid; g < G; g += nthr) {
+    const int64_t lo = worker_begin(g, T, G), hi = worker_begin(g + 1, T, G);
+    if (hi > lo) {
+      const int segs = seq_of_tile(pre, B, hi - 1) - seq_of_tile(pre, B, lo) + 1;
+      cb = max(cb, (hi - lo) + (int64_t)kSegPenaltyTiles * (segs - 1));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ca = max(ca, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)ca, o));
+    cb = max(cb, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)cb, o));
+  }
+  __shared__ long long red[2][32];
+  __shared__ int s_pick;
+  if (lane == 0) {
+    red[0][warp] = ca;
+    red[1][warp] = cb;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    long long a = 0, c = 0;
+    for (int w = 0; w < (nthr + 31) / 32; ++w) {
+      a = max(a, red[0][w]);
+      c = max(c, red[1][w]);
+    }
+    s_pick = a <= c;
+  }
+  __syncthreads();
+  return s_pick != 0;
+}
+
 }  // namespace mla
