@@ -155,6 +155,52 @@ def _isnum(s):
         return False
 
 
+def other_configs(torch, mi, mla, dev, K: int = 30):
+    """The decode call alone on the other 128-head configurations (ragged paged
+    batch, long context), graph-timed; their caches exceed L2.  Supporting
+    figures: the headline metric is the V3 step above."""
+    out = {}
+    peaks = load_peaks()
+    for name in ("paged", "long"):
+        wl = mi.make(name, poison=False)
+        dims = mla.Dims.of(wl)
+        to = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev).view(torch.bfloat16)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).to(dev)
+        pool, q, sl = to(wl.pool), to(wl.q), i32(wl.seqlens)
+        bt = i32(wl.block_table) if wl.paged else None
+        ws = torch.empty(mla.mla_decode_workspace_size(dims, wl.batch, 0), dtype=torch.uint8, device=dev)
+        z = torch.empty((wl.batch, wl.n_heads, wl.d_latent), dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def call():
+            mla.mla_decode_attn(dims, q, pool, sl, wl.scale, block_table=bt, num_blocks=wl.num_blocks,
+                                seq_stride=wl.seq_stride, workspace=ws, z_out=z, want_lse=False, dev_status=status)
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        for _ in range(5):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if mla.mla_read_status(status) != 0:
+            raise RuntimeError(f"device status during the {name} decode timing")
+        us = e0.elapsed_time(e1) * 1e3 / K
+        alg = algorithmic(wl)
+        gbs = alg["bytes"] / (us * 1e-6) / 1e9
+        out[name] = {"decode_us": round(us, 2), "batch": wl.batch, "tokens": alg["tokens"], "hbm_gbs": round(gbs, 1),
+                     "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "tflops": round(alg["flops"] / (us * 1e-6) / 1e12, 1)}
+        del pool, q, ws, z
+        torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -335,6 +381,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_us = e0.elapsed_time(e1) * 1e3 / K
     if sampler:
         sampler.stop()
+    others = other_configs(torch, mi, mla, dev) if (rank == 0 and not args.no_others) else None
 
     if rank != 0:
         if dist is not None:
@@ -376,6 +423,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "path": "eager public API calls; the packed inputs copied in from one pinned host buffer, the output copied out"},
         "timing": "CUDA-graph replay of each step (one graph per rotating layer copy), CUDA events",
+        "other_configs": others,
         "gpu_launches": K * sum(LAUNCHES_PER_STEP.values()),
         "clocks": sampler.summary() if sampler else None,
     }
@@ -467,6 +515,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-others", action="store_true", help="skip the paged / long decode figures")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(1)))
