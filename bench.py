@@ -156,12 +156,13 @@ def _isnum(s):
 
 
 def other_configs(torch, mi, mla, dev, K: int = 30):
-    """The decode call alone on the other 128-head configurations (ragged paged
-    batch, long context), graph-timed; their caches exceed L2.  Supporting
-    figures: the headline metric is the V3 step above."""
+    """The decode call alone on the other configurations, graph-timed: the
+    128-head ragged paged batch and long context (tensor-core kernel) and the
+    16-head low-head batch (shape-generic kernel); their caches exceed L2.
+    Supporting figures: the headline metric is the V3 step above."""
     out = {}
     peaks = load_peaks()
-    for name in ("paged", "long"):
+    for name in ("paged", "long", "lowhead"):
         wl = mi.make(name, poison=False)
         dims = mla.Dims.of(wl)
         to = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -515,7 +516,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--no-others", action="store_true", help="skip the paged / long decode figures")
+    ap.add_argument("--no-others", action="store_true", help="skip the paged / long / low-head decode figures")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(1)))

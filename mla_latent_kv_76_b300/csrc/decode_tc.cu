@@ -209,8 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
   tile_prefix(p.seqlens, p.batch, cap, p.status, pre, kTile);  // ends with __syncthreads
   int* Wp = pre + p.batch + 1;                                  // entries prefix of the split plan
-  plan_prefix(pre, p.batch, p.workers, Wp);                     // ends with __syncthreads
-  const bool aligned = prefer_aligned_plan(pre, Wp, p.batch, p.workers);
+  const bool aligned = plan_prefix(pre, p.batch, p.workers, Wp);  // ends with __syncthreads
   if (blockIdx.x == 0 && tid == 0) *p.plan_flag = aligned ? 1 : 0;
   tc::tc_fence_before();
   tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival

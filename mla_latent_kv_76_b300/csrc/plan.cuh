@@ -10,6 +10,8 @@
 // workers g_first(b) .. g_last(b) whose range meets b's tiles.
 #pragma once
 
+#include <climits>
+
 #include <stdint.h>
 
 #include "common.cuh"
@@ -100,39 +102,75 @@ MLA_DEVI int entry_start(int k, int t, int w) { return (int)((int64_t)t * k / w)
 MLA_DEVI int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau + 1) * w - 1) / t); }
 
 // Exclusive prefix of plan_entries over b into W[0..B] (shared memory), from the
-// tile prefix pre[0..B]; every thread of the block takes part.
-MLA_DEVI void plan_prefix(const int* pre, int B, int G, int* W) {
+// tile prefix pre[0..B]; every thread of the block takes part and gets the same
+// return value: whether the sequence-aligned plan is preferred over the even
+// split of the tile list.  The aligned plan costs its longest entry (tiles); the
+// even split costs at most Q + kSegPenaltyTiles * ceil(Q / t_min) (Q = ceil(T/G)
+// tiles per worker, t_min the shortest non-empty sequence; a worker can meet at
+// most that many sequence boundaries, and each extra sequence costs one more
+// partial write and a query reload, ~kSegPenaltyTiles tile times).  Uniform
+// batches keep the aligned plan (16 x 4096: 8 vs 10); many ragged sequences take
+// the even split (64 sequences of 1024..8192 tokens: 64 vs 48).
+constexpr int kSegPenaltyTiles = 3;
+MLA_DEVI bool plan_prefix(const int* pre, int B, int G, int* W) {
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int per = (B + nthr - 1) / nthr;
   const int b0 = tid * per, b1 = min(B, b0 + per);
-  __shared__ int red[32];
-  __shared__ int s_n;
-  int n = 0;
-  for (int b = b0; b < b1; ++b) n += pre[b + 1] > pre[b];
+  __shared__ int red[32], redmin[32], redmax[32];
+  __shared__ int s_n, s_tmin;
+  int n = 0, tmin = INT_MAX;
+  for (int b = b0; b < b1; ++b) {
+    const int t = pre[b + 1] - pre[b];
+    if (t > 0) {
+      ++n;
+      tmin = min(tmin, t);
+    }
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-  if (lane == 0) red[warp] = n;
+  for (int o = 16; o > 0; o >>= 1) {
+    n += __shfl_xor_sync(0xffffffffu, n, o);
+    tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+  }
+  if (lane == 0) {
+    red[warp] = n;
+    redmin[warp] = tmin;
+  }
   __syncthreads();
   if (tid == 0) {
-    int t = 0;
-    for (int w = 0; w < (nthr + 31) / 32; ++w) t += red[w];
+    int t = 0, m = INT_MAX;
+    for (int w = 0; w < (nthr + 31) / 32; ++w) {
+      t += red[w];
+      m = min(m, redmin[w]);
+    }
     s_n = t;
+    s_tmin = m;
   }
   __syncthreads();
   const int64_t T = pre[B];
-  int local = 0;
-  for (int b = b0; b < b1; ++b) local += plan_entries(pre[b + 1] - pre[b], T, s_n, G);
+  int local = 0, lmax = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int t = pre[b + 1] - pre[b];
+    const int w = plan_entries(t, T, s_n, G);
+    local += w;
+    if (w > 0) lmax = max(lmax, (t + w - 1) / w);
+  }
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
   __syncthreads();  // red[] is reused
   if (lane == 31) red[warp] = incl;
+  if (lane == 0) redmax[warp] = lmax;
   __syncthreads();
-  int warp_off = 0;
-  for (int w = 0; w < warp; ++w) warp_off += red[w];
+  int warp_off = 0, cost_aligned = 0;
+  for (int w = 0; w < (nthr + 31) / 32; ++w) {
+    if (w < warp) warp_off += red[w];
+    cost_aligned = max(cost_aligned, redmax[w]);
+  }
   int run = warp_off + incl - local;
   for (int b = b0; b < b1; ++b) {
     W[b] = run;
@@ -140,6 +178,10 @@ MLA_DEVI void plan_prefix(const int* pre, int B, int G, int* W) {
   }
   if (tid == nthr - 1) W[B] = run;
   __syncthreads();
+  if (T == 0) return true;
+  const int64_t q = (T + G - 1) / G;
+  const int64_t cost_split = q + (int64_t)kSegPenaltyTiles * ((q + s_tmin - 1) / s_tmin);
+  return cost_aligned <= cost_split;
 }
 
 // The sequence owning entry e < W[B]: the largest b with W[b] <= e.
@@ -151,54 +193,6 @@ MLA_DEVI int64_t entry_tile(const int* pre, const int* W, int B, int64_t e) {
   const int b = seq_of_entry(W, B, e);
   const int t = pre[b + 1] - pre[b], w = W[b + 1] - W[b];
   return pre[b] + entry_start((int)(e - W[b]), t, w);
-}
-
-// Which plan a tensor-core decode call uses.  The sequence-aligned plan costs its
-// longest entry (tiles); the even split of the tile list costs its most
-// expensive worker, tiles + kSegPenaltyTiles per sequence beyond the first (each
-// extra sequence costs one more partial write and a query reload, ~3 tiles of
-// time).  The aligned plan wins on uniform batches (16 x 4096: 8 vs 10); the
-// even split wins when sequences outnumber half the workers and their lengths
-// vary (64 sequences of 1024..8192 tokens: 64 vs 40).  Every thread of the block
-// gets the same answer.
-constexpr int kSegPenaltyTiles = 3;
-MLA_DEVI bool prefer_aligned_plan(const int* pre, const int* W, int B, int G) {
-  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t T = pre[B];
-  int64_t ca = 0, cb = 0;
-  for (int b = tid; b < B; b += nthr) {
-    const int t = pre[b + 1] - pre[b], w = W[b + 1] - W[b];
-    if (t > 0 && w > 0) ca = max(ca, (int64_t)((t + w - 1) / w));
-  }
-  for (int g = tid; g < G; g += nthr) {
-    const int64_t lo = worker_begin(g, T, G), hi = worker_begin(g + 1, T, G);
-    if (hi > lo) {
-      const int segs = seq_of_tile(pre, B, hi - 1) - seq_of_tile(pre, B, lo) + 1;
-      cb = max(cb, (hi - lo) + (int64_t)kSegPenaltyTiles * (segs - 1));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ca = max(ca, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)ca, o));
-    cb = max(cb, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)cb, o));
-  }
-  __shared__ long long red[2][32];
-  __shared__ int s_pick;
-  if (lane == 0) {
-    red[0][warp] = ca;
-    red[1][warp] = cb;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    long long a = 0, c = 0;
-    for (int w = 0; w < (nthr + 31) / 32; ++w) {
-      a = max(a, red[0][w]);
-      c = max(c, red[1][w]);
-    }
-    s_pick = a <= c;
-  }
-  __syncthreads();
-  return s_pick != 0;
 }
 
 }  // namespace mla
