@@ -1,13 +1,17 @@
 // Split-KV work partition shared by the decode partial kernels and the combine.
 //
-// Every sequence b is cut into ceil(L_b / 64) tiles; the tiles of all
-// sequences, in batch order, form one list of T tiles.  Worker g of G owns
-// the contiguous range [floor(g T / G), floor((g+1) T / G)), which may cover
-// the end of one sequence and the start of the next.  Each (worker, sequence)
-// segment writes one partial (o, lse) to slot g + b; slots are unique because
-// worker ranges are ordered (if worker g touches sequence b, worker g + 1
-// starts at b or later).  The combine merges, for sequence b, the slots of
-// workers g_first(b) .. g_last(b) whose range meets b's tiles.
+// Even split (both decode paths): every sequence b is cut into tiles (64 tokens
+// on the shape-generic path, 128 on the tensor-core path); the tiles of all
+// sequences, in batch order, form one list of T tiles.  Worker g of G owns the
+// contiguous range [floor(g T / G), floor((g+1) T / G)), which may cover the end
+// of one sequence and the start of the next.  Each (worker, sequence) segment
+// writes one partial to slot g + b; slots are unique because worker ranges are
+// ordered (if worker g touches sequence b, worker g + 1 starts at b or later).
+// The combine merges, for sequence b, the slots of workers g_first(b) ..
+// g_last(b) whose range meets b's tiles.
+//
+// Sequence-aligned plan (tensor-core path, chosen per call when cheaper): see
+// plan_entries / plan_prefix below.
 #pragma once
 
 #include <climits>
