@@ -20,8 +20,9 @@
 // re-reads the latent columns a few microseconds later, from L2.
 //
 // Score CTA, 384 threads: warp 0 TMA (3 ring slots, each three 64-column
-// chunks of 128 tokens, 128-byte swizzle; lane c issues chunk c), warp 1 MMA issue (S double-buffered
-// in TMEM; one barrier wait and one commit per 12 MMAs),
+// chunks of 128 tokens, 128-byte swizzle; lane c issues chunk c; the first
+// segment's query arrives through the ring ahead of tile 0), warp 1 MMA issue
+// (S double-buffered in TMEM; one barrier wait and one commit per 12 MMAs),
 // warps 4-7 / 8-11 softmax for token columns 0-63 / 64-127 (thread = head),
 // warps 2 / 3 ship each warpgroup's P to the value CTA as one bulk copy.
 // Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns; lane c issues
