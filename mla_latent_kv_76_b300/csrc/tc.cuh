@@ -251,9 +251,13 @@ MLA_DEVI void mbar_arrive_cluster_addr_relaxed(uint32_t remote_bar) {
 // engine.  Arrives on the destination's barrier with the byte count as
 // expected transactions; the copy completes that count, so the destination
 // sees the data once the barrier phase completes.  (The source buffer may be
-// reused only after the destination has reported completion.)
+// reused only after the destination has reported completion.)  The arrive is
+// relaxed: the data travels with the copy's complete_tx, and the phase cannot
+// complete before this arrival lands even if the copy's bytes land first (the
+// transaction count may go below zero meanwhile, as with multicast loads into
+// a peer).  A cluster-scope release here held the issuing thread ~1.5 us.
 MLA_DEVI void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t dst_bar) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(dst_bar), "r"(bytes)
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(dst_bar), "r"(bytes)
                : "memory");
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "r"(smem_u32(src)), "r"(bytes), "r"(dst_bar)
