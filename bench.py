@@ -372,14 +372,19 @@ def run_ours(args, rank, world, local_rank):
     for i in range(3):
         e2e_step(i)
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(K):
-        e2e_step(k)
-    e1.record(stream)
-    barrier()
-    e2e_us = e0.elapsed_time(e1) * 1e3 / K
+    # the eager path is bound by host-side work, which other tenants of the host
+    # can disturb: three timed runs of K steps, the median reported
+    e2e_runs = []
+    for _ in range(3):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(K):
+            e2e_step(k)
+        e1.record(stream)
+        barrier()
+        e2e_runs.append(e0.elapsed_time(e1) * 1e3 / K)
+    e2e_us = statistics.median(e2e_runs)
     if sampler:
         sampler.stop()
     others = other_configs(torch, mi, mla, dev) if (rank == 0 and not args.no_others) else None
@@ -422,6 +427,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "runs": [round(x, 1) for x in e2e_runs],
                 "path": "eager public API calls; the packed inputs copied in from one pinned host buffer, the output copied out"},
         "timing": "CUDA-graph replay of each step (one graph per rotating layer copy), CUDA events",
         "other_configs": others,
