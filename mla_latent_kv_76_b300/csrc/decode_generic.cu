@@ -17,6 +17,7 @@
 namespace mla {
 
 constexpr int kHG = 16;          // heads per CTA (one m16 block)
+constexpr int kMaxWarps = 8;     // warps per CTA: 8 for d_c >= 128, 4 for d_c = 64
 constexpr int kPRow = 64 * 2 + 16;  // staged P row: 144 B (9 chunks)
 
 struct GenericSmem {
@@ -32,15 +33,23 @@ __host__ __device__ inline GenericSmem generic_smem(int D, int batch) {
   s.off_kv1 = s.off_kv0 + kTileTokens * s.row_bytes;
   s.off_p = s.off_kv1 + kTileTokens * s.row_bytes;
   s.off_red = s.off_p + kHG * kPRow;
-  s.off_prefix = s.off_red + 3 * 4 * kHG * 4;
+  s.off_prefix = s.off_red + 3 * kMaxWarps * kHG * 4;
   s.total = s.off_prefix + ((batch + 1) * 4 + 15) / 16 * 16;
   return s;
 }
 
 int generic_head_groups(int n_heads) { return (n_heads + kHG - 1) / kHG; }
 
-template <int DC>
-__global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch a) {
+MLA_DEVI void ldsm_x2_b(uint32_t (&r)[2], const void* smem_ptr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r[0]), "=r"(r[1]) : "r"(smem_u32(smem_ptr)));
+}
+
+// NW warps: in the score each warp takes 64 / NW tokens of the tile, in the
+// weighted sum DC / NW latent columns.  Eight warps halve the serial chain of
+// mma.sync / ldmatrix / softmax steps each warp issues per tile (with four, a
+// 16-head batch ran issue-bound at a third of DRAM peak).
+template <int DC, int NW>
+__global__ void __launch_bounds__(NW * 32) decode_generic_kernel(const DecodeLaunch a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int D = DC + a.d_rope;
   const GenericSmem L = generic_smem(D, a.batch);
@@ -48,8 +57,11 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
   uint8_t* sQ = smem + L.off_q;
   uint8_t* sKV[2] = {smem + L.off_kv0, smem + L.off_kv1};
   uint8_t* sP = smem + L.off_p;
-  float* sMax = reinterpret_cast<float*>(smem + L.off_red);  // [4][16]
-  float* sSum = sMax + 4 * kHG;                                // [4][16]
+  float* sMax = reinterpret_cast<float*>(smem + L.off_red);  // [NW][16]
+  float* sSum = sMax + NW * kHG;                               // [NW][16]
+  constexpr int TPW = kTileTokens / NW;  // score tokens per warp
+  constexpr int SB = TPW / 8;            // n8 blocks per warp in the score
+  static_assert(SB == 1 || SB == 2, "4 or 8 warps");
   int* pre = reinterpret_cast<int*>(smem + L.off_prefix);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -82,7 +94,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
 
     __syncthreads();  // previous segment finished with sQ / sKV
     // query rows of this head group (rows past n_heads are zero)
-    for (int c = tid; c < kHG * chunks; c += 128) {
+    for (int c = tid; c < kHG * chunks; c += NW * 32) {
       const int r = c / chunks, ch = c % chunks, h = hg * kHG + r;
       const bool ok = h < a.n_heads;
       cp_async16(sQ + r * RS + ch * 16, ok ? qg + ((int64_t)b * a.n_heads + h) * D + ch * 8 : qg, ok);
@@ -100,7 +112,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
       } else {
         base = pool + ((int64_t)b * a.seq_stride + t0) * D;
       }
-      for (int r = warp; r < kTileTokens; r += 4) {
+      for (int r = warp; r < kTileTokens; r += NW) {
         const bool ok = blk_ok && (t0 + r < Lb);
         for (int ch = lane; ch < chunks; ch += 32)
           cp_async16(sKV[buf] + r * RS + ch * 16, ok ? base + (int64_t)r * D + ch * 8 : pool, ok);
@@ -110,7 +122,8 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
     cp_async_commit();
 
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    constexpr int NB = DC / 32;  // n8 blocks of the latent per warp
+    constexpr int NB = DC / (8 * NW);  // n8 blocks of the latent per warp
+    static_assert(NB >= 2 && NB % 2 == 0, "value columns are loaded two n8 blocks at a time");
     float o[NB][4];
 #pragma unroll
     for (int i = 0; i < NB; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -128,24 +141,36 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
       const uint8_t* kv = sKV[buf];
       const int t0 = (t_begin + j) * kTileTokens;
 
-      // ---- score: warp owns tokens [16 warp, 16 warp + 16) of the tile
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // ---- score: warp owns tokens [TPW warp, TPW warp + TPW) of the tile
+      float s[SB][4];
+#pragma unroll
+      for (int nb = 0; nb < SB; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
       const uint8_t* qa = sQ + (lane & 15) * RS + (lane >> 4) * 16;
-      const uint8_t* kb = kv + (warp * 16 + (lane & 7) + (lane >> 4) * 8) * RS + ((lane >> 3) & 1) * 16;
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t af[4], bf[4];
-        ldsm_x4(af, qa + kk * 32);
-        ldsm_x4(bf, kb + kk * 32);
-        mma_bf16(s[0], af, bf[0], bf[1]);
-        mma_bf16(s[1], af, bf[2], bf[3]);
+      if (SB == 2) {
+        const uint8_t* kb = kv + (warp * 16 + (lane & 7) + (lane >> 4) * 8) * RS + ((lane >> 3) & 1) * 16;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t af[4], bf[4];
+          ldsm_x4(af, qa + kk * 32);
+          ldsm_x4(bf, kb + kk * 32);
+          mma_bf16(s[0], af, bf[0], bf[1]);
+          mma_bf16(s[SB - 1], af, bf[2], bf[3]);
+        }
+      } else {
+        const uint8_t* kb = kv + (warp * 8 + (lane & 7)) * RS + ((lane >> 3) & 1) * 16;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t af[4], bf[2];
+          ldsm_x4(af, qa + kk * 32);
+          ldsm_x2_b(bf, kb + kk * 32);
+          mma_bf16(s[0], af, bf[0], bf[1]);
+        }
       }
       // ---- scale, mask, tile row max
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
+      for (int nb = 0; nb < SB; ++nb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int tok = t0 + warp * 16 + nb * 8 + tq * 2 + (e & 1);
+          const int tok = t0 + warp * TPW + nb * 8 + tq * 2 + (e & 1);
           const float v = (tok < Lb) ? s[nb][e] * sl2 : -INFINITY;
           s[nb][e] = v;
           mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -165,7 +190,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
       for (int r = 0; r < 2; ++r) {
         float tm = sMax[gq + 8 * r];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) tm = fmaxf(tm, sMax[w * kHG + gq + 8 * r]);
+        for (int w = 1; w < NW; ++w) tm = fmaxf(tm, sMax[w * kHG + gq + 8 * r]);
         const float mn = fmaxf(m_run[r], tm);
         alpha[r] = exp2f(m_run[r] - mn);
         m_run[r] = mn;
@@ -173,7 +198,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
       }
       // ---- P = 2^(x - m), rounded to bf16 (the same weights feed the sum and l)
 #pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
+      for (int nb = 0; nb < SB; ++nb)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const float p0 = exp2f(s[nb][2 * r] - m_run[r]);
@@ -181,7 +206,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
           const uint32_t pk = pack_bf16x2(p0, p1);
           const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pk);
           l_run[r] += __low2float(pb) + __high2float(pb);
-          *reinterpret_cast<uint32_t*>(sP + (gq + 8 * r) * kPRow + (warp * 16 + nb * 8 + tq * 2) * 2) = pk;
+          *reinterpret_cast<uint32_t*>(sP + (gq + 8 * r) * kPRow + (warp * TPW + nb * 8 + tq * 2) * 2) = pk;
         }
       __syncthreads();
       // ---- O = alpha O + P . C[:, warp's latent columns]
@@ -192,7 +217,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
         o[i][2] *= alpha[1];
         o[i][3] *= alpha[1];
       }
-      const int d_warp = warp * (DC / 4);
+      const int d_warp = warp * (DC / NW);
 #pragma unroll
       for (int kk = 0; kk < kTileTokens / 16; ++kk) {
         uint32_t af[4];
@@ -224,11 +249,12 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeLaunch 
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int h = hg * kHG + gq + 8 * r;
-      const float l = sSum[gq + 8 * r] + sSum[kHG + gq + 8 * r] + sSum[2 * kHG + gq + 8 * r] +
-                      sSum[3 * kHG + gq + 8 * r];
+      float l = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) l += sSum[w * kHG + gq + 8 * r];
       if (h >= a.n_heads) continue;
       const float inv = 1.f / l;
-      float* op = a.o_part + (slot * a.n_heads + h) * DC + warp * (DC / 4) + tq * 2;
+      float* op = a.o_part + (slot * a.n_heads + h) * DC + warp * (DC / NW) + tq * 2;
 #pragma unroll
       for (int i = 0; i < NB; ++i)
         *reinterpret_cast<float2*>(op + i * 8) = make_float2(o[i][2 * r] * inv, o[i][2 * r + 1] * inv);
@@ -317,11 +343,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeLaunch a) {
 
 template <int DC>
 static cudaError_t launch_generic_dc(const DecodeLaunch& a, cudaStream_t s) {
+  constexpr int NW = DC >= 128 ? 8 : 4;
   const GenericSmem L = generic_smem(DC + a.d_rope, a.batch);
-  cudaError_t e = ensure_smem<decode_generic_kernel<DC>>(L.total);
+  cudaError_t e = ensure_smem<decode_generic_kernel<DC, NW>>(L.total);
   if (e != cudaSuccess) return e;
   dim3 grid(a.workers, generic_head_groups(a.n_heads));
-  decode_generic_kernel<DC><<<grid, 128, L.total, s>>>(a);
+  decode_generic_kernel<DC, NW><<<grid, NW * 32, L.total, s>>>(a);
   return cudaGetLastError();
 }
 
