@@ -203,6 +203,23 @@ def other_configs(torch, mi, mla, dev, K: int = 30):
 
 
 # --------------------------------------------------------------------------- our arm
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest `x` over all ranks (every rank gets it); `x` itself when
+    there is no process group.  Replicas are timed independently and the job
+    is as slow as its slowest rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(batch: int, world: int, us_per_step: float) -> float:
+    """Whole-job throughput: every replica decodes `batch` sequences per step."""
+    return batch * world / (us_per_step * 1e-6)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import mla_inputs as mi
@@ -339,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
         g_dec[k % ROTATE].replay()
     d1.record(stream)
     barrier()
-    dec_us_list = [d0.elapsed_time(d1) * 1e3 / K]
+    dec_us_list = [max_over_ranks(d0.elapsed_time(d1) * 1e3 / K, dist, dev)]
     # post-roll for the sampler
     t_end = time.time() + (0.3 if sampler else 0.0)
     while time.time() < t_end:
@@ -351,11 +368,7 @@ def run_ours(args, rank, world, local_rank):
     st = mla.mla_read_status(status)
     if st != 0:
         raise RuntimeError(f"device status {st} during the benchmark")
-    us_per_step = total_ms * 1e3 / K
-    if dist is not None:
-        t = torch.tensor([us_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us_per_step = float(t.item())
+    us_per_step = max_over_ranks(total_ms * 1e3 / K, dist, dev)
 
     # ---- end to end through the public API with host buffers: every step copies
     # its packed inputs from pinned host memory and reads the output back
@@ -384,7 +397,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         barrier()
         e2e_runs.append(e0.elapsed_time(e1) * 1e3 / K)
-    e2e_us = statistics.median(e2e_runs)
+    e2e_us = max_over_ranks(statistics.median(e2e_runs), dist, dev)
     if sampler:
         sampler.stop()
     others = other_configs(torch, mi, mla, dev) if (rank == 0 and not args.no_others) else None
@@ -414,13 +427,12 @@ def run_ours(args, rank, world, local_rank):
             "roofline_time_us": round(max(t_hbm, t_tc) * 1e6, 2),
             "roofline_frac": round(max(t_hbm, t_tc) * 1e6 / dec_us, 4)}
     cpu = cpu_baseline(wl, args.cpu_seconds) if not args.no_cpu else None
-    world_tokens = wl.batch * world
     line = {
         "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(us_per_step / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), random-init weights)",
         "config": dict(workload_desc(wl), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-        "tokens_per_s": round(world_tokens / (us_per_step * 1e-6), 1),
+        "tokens_per_s": round(job_tokens_per_s(wl.batch, world, us_per_step), 1),
         "decode": {"us": round(dec_us, 3), "timing": "CUDA-graph replays of the decode call alone, same rotation",
                    "hbm_gbs": round(dec_gbs, 1), "tflops": round(dec_tfs, 1),
                    "tokens_per_s": round(wl.batch / (dec_us * 1e-6), 1)},
