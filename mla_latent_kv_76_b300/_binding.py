@@ -96,6 +96,16 @@ def _ptr(t: Optional[torch.Tensor], name: str, dtypes=None) -> Optional[int]:
     return t.data_ptr()
 
 
+def _need(t: Optional[torch.Tensor], n: int, name: str) -> None:
+    """The library sees only pointers: refuse a buffer smaller than the call
+    will read or write through it."""
+    if t is not None and isinstance(t, torch.Tensor) and t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call needs at least {n}")
+
+
+_Z_DTYPES = (torch.float32,) + _BF16_LIKE
+
+
 def _stream(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -113,6 +123,12 @@ def mla_absorb_q(dims: Dims, q_c, q_r, pos, w_uk, q_out=None, stream=None):
     if q_out is None:
         q_out = torch.empty((B, dims.n_heads, dims.d_latent + dims.d_rope), dtype=torch.bfloat16,
                             device=q_c.device)
+    H = B * dims.n_heads
+    _need(q_c, H * dims.d_head, "q_c")
+    _need(q_r, H * dims.d_rope, "q_r")
+    _need(pos, B, "pos")
+    _need(w_uk, dims.n_heads * dims.d_head * dims.d_latent, "w_uk")
+    _need(q_out, H * (dims.d_latent + dims.d_rope), "q_out")
     code = lib.mla_absorb_q(ctypes.byref(dims), B, _ptr(q_c, "q_c", _BF16_LIKE), _ptr(q_r, "q_r", _BF16_LIKE),
                             _ptr(pos, "pos", (torch.int32,)), _ptr(w_uk, "w_uk", _BF16_LIKE),
                             _ptr(q_out, "q_out", _BF16_LIKE), _stream(stream))
@@ -125,6 +141,15 @@ def mla_append_cache(dims: Dims, h, w_dkv_kr, seq_idx, pos, pool, n_seqs: int, b
     """Project h through [W^DKV; W^KR], RoPE the k^R part, write bf16 rows into `pool` in place."""
     T, d_model = h.shape
     max_blocks = 0 if block_table is None else block_table.shape[1]
+    D = dims.d_latent + dims.d_rope
+    _need(w_dkv_kr, D * d_model, "w_dkv_kr")
+    _need(seq_idx, T, "seq_idx")
+    _need(pos, T, "pos")
+    if block_table is not None:
+        _need(block_table, n_seqs * max_blocks, "block_table")
+        _need(pool, num_blocks * dims.block_tokens * D, "pool")
+    else:
+        _need(pool, n_seqs * seq_stride * D, "pool")
     code = lib.mla_append_cache(ctypes.byref(dims), T, d_model, _ptr(h, "h", _BF16_LIKE),
                                 _ptr(w_dkv_kr, "w_dkv_kr", _BF16_LIKE), _ptr(seq_idx, "seq_idx", (torch.int32,)),
                                 _ptr(pos, "pos", (torch.int32,)), n_seqs,
@@ -137,6 +162,23 @@ def mla_append_cache(dims: Dims, h, w_dkv_kr, seq_idx, pos, pool, n_seqs: int, b
 
 def mla_decode_workspace_size(dims: Dims, batch: int, num_workers: int = 0) -> int:
     return int(lib.mla_decode_workspace_size(ctypes.byref(dims), batch, num_workers))
+
+
+def _check_decode_buffers(dims, B, q, pool, seqlens, block_table, max_blocks, num_blocks, seq_stride, z_out,
+                          lse_out) -> None:
+    D = dims.d_latent + dims.d_rope
+    H = B * dims.n_heads
+    _need(q, H * D, "q")
+    _need(seqlens, B, "seqlens")
+    if block_table is not None:
+        _need(block_table, B * max_blocks, "block_table")
+        _need(pool, num_blocks * dims.block_tokens * D, "pool")
+    else:
+        _need(pool, B * seq_stride * D, "pool")
+    if z_out is not None and z_out.dtype not in _Z_DTYPES:
+        raise TypeError(f"z_out has dtype {z_out.dtype}, expected float32 or bf16")
+    _need(z_out, H * dims.d_latent, "z_out")
+    _need(lse_out, H, "lse_out")
 
 
 def mla_decode_attn(dims: Dims, q, pool, seqlens, scale: float, block_table=None, num_blocks: int = 0,
@@ -157,6 +199,7 @@ def mla_decode_attn(dims: Dims, q, pool, seqlens, scale: float, block_table=None
     if lse_out is None and want_lse:
         lse_out = torch.empty((B, dims.n_heads), dtype=torch.float32, device=dev)
     max_blocks = 0 if block_table is None else block_table.shape[1]
+    _check_decode_buffers(dims, B, q, pool, seqlens, block_table, max_blocks, num_blocks, seq_stride, z_out, lse_out)
     code = lib.mla_decode_attn(
         ctypes.byref(dims), B, _ptr(q, "q", _BF16_LIKE), _ptr(pool, "pool", _BF16_LIKE),
         _ptr(block_table, "block_table", (torch.int32,)), max_blocks, num_blocks, seq_stride,
@@ -184,6 +227,7 @@ def mla_decode_attn_noalloc(dims: Dims, q, pool, seqlens, scale: float, block_ta
     if lse_out is None and want_lse:
         lse_out = torch.empty((B, dims.n_heads), dtype=torch.float32, device=dev)
     max_blocks = 0 if block_table is None else block_table.shape[1]
+    _check_decode_buffers(dims, B, q, pool, seqlens, block_table, max_blocks, num_blocks, seq_stride, z_out, lse_out)
     code = lib.mla_decode_attn_noalloc(
         ctypes.byref(dims), B, _ptr(q, "q", _BF16_LIKE), _ptr(pool, "pool", _BF16_LIKE),
         _ptr(block_table, "block_table", (torch.int32,)), max_blocks, num_blocks, seq_stride,
@@ -200,6 +244,9 @@ def mla_out_proj(dims: Dims, z, w_uv, o_out=None, stream=None):
     B = z.shape[0]
     if o_out is None:
         o_out = torch.empty((B, dims.n_heads, dims.d_v), dtype=torch.bfloat16, device=z.device)
+    _need(z, B * dims.n_heads * dims.d_latent, "z")
+    _need(w_uv, dims.n_heads * dims.d_v * dims.d_latent, "w_uv")
+    _need(o_out, B * dims.n_heads * dims.d_v, "o_out")
     code = lib.mla_out_proj(ctypes.byref(dims), B, _ptr(z, "z", _BF16_LIKE), _ptr(w_uv, "w_uv", _BF16_LIKE),
                             _ptr(o_out, "o_out", _BF16_LIKE), _stream(stream))
     _check("mla_out_proj", code)

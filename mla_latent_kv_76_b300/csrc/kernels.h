@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "../../include/mla.h"
 
@@ -13,14 +14,21 @@ namespace mla {
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device.  Done once per (kernel, device) and size increase, so that
 // steady-state launches make no host API call besides the launch itself.
+// The slow path runs under a lock and only ever raises the limit, so host
+// threads racing with different sizes cannot record a size above the one set.
 template <auto Kernel>
 cudaError_t ensure_smem(int bytes) {
   static std::atomic<int> set_bytes[64];
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (dev >= 0 && dev < 64 && bytes <= set_bytes[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && bytes <= set_bytes[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(mu);
+  const int have = cached ? set_bytes[dev].load(std::memory_order_relaxed) : 0;
+  if (bytes <= have) return cudaSuccess;
   const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) set_bytes[dev].store(bytes, std::memory_order_relaxed);
+  if (e == cudaSuccess && cached) set_bytes[dev].store(bytes, std::memory_order_release);
   return e;
 }
 

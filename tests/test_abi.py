@@ -163,3 +163,53 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import mla_latent_kv_76_b300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "libmla.so is missing" in r.stderr
+
+
+def test_binding_refuses_undersized_buffers(mla):
+    """The C ABI sees only pointers, so the binding checks every buffer against
+    the element count the call will touch before anything is launched (these
+    tensors live on the host: the size check comes first)."""
+    import torch
+    d = _dims(mla, n_heads=4, d_head=8, d_v=8, d_latent=64, d_rope=16)
+    bf = dict(dtype=torch.bfloat16)
+    B, D = 2, 80
+    ok_q = torch.zeros(B, 4, D, **bf)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    sl = torch.ones(B, dtype=torch.int32)
+
+    def raises(fn, name):
+        with pytest.raises(ValueError, match=name + " holds"):
+            fn()
+    raises(lambda: mla.mla_absorb_q(d, torch.zeros(B, 4, 8, **bf), torch.zeros(B, 4, 16, **bf),
+                                    torch.zeros(B, dtype=torch.int32), torch.zeros(4, 8, 63, **bf)), "w_uk")
+    raises(lambda: mla.mla_absorb_q(d, torch.zeros(B, 4, 7, **bf), torch.zeros(B, 4, 16, **bf),
+                                    torch.zeros(B, dtype=torch.int32), torch.zeros(4, 8, 64, **bf)), "q_c")
+    raises(lambda: mla.mla_decode_attn(d, ok_q[:, :3], torch.zeros(B, 8, D, **bf), sl, 0.1, seq_stride=8,
+                                       workspace=ws), "q")
+    raises(lambda: mla.mla_decode_attn(d, ok_q, torch.zeros(B, 7, D, **bf), sl, 0.1, seq_stride=8,
+                                       workspace=ws), "pool")
+    raises(lambda: mla.mla_decode_attn(d, ok_q, torch.zeros(B, 8, D, **bf), sl[:1], 0.1, seq_stride=8,
+                                       workspace=ws), "seqlens")
+    raises(lambda: mla.mla_decode_attn(d, ok_q, torch.zeros(5, 64, D, **bf), sl, 0.1, workspace=ws,
+                                       block_table=torch.zeros(B, 3, dtype=torch.int32), num_blocks=6), "pool")
+    raises(lambda: mla.mla_decode_attn(d, ok_q, torch.zeros(B, 8, D, **bf), sl, 0.1, seq_stride=8, workspace=ws,
+                                       z_out=torch.zeros(B, 4, 63)), "z_out")
+    raises(lambda: mla.mla_decode_attn(d, ok_q, torch.zeros(B, 8, D, **bf), sl, 0.1, seq_stride=8, workspace=ws,
+                                       lse_out=torch.zeros(B, 3)), "lse_out")
+    with pytest.raises(TypeError, match="z_out"):
+        mla.mla_decode_attn(d, ok_q, torch.zeros(B, 8, D, **bf), sl, 0.1, seq_stride=8, workspace=ws,
+                            z_out=torch.zeros(B, 4, 64, dtype=torch.int32))
+    raises(lambda: mla.mla_append_cache(d, torch.zeros(3, 16, **bf), torch.zeros(D, 16, **bf),
+                                        torch.zeros(3, dtype=torch.int32), torch.zeros(3, dtype=torch.int32),
+                                        torch.zeros(2, 8, D - 1, **bf), n_seqs=2, seq_stride=8), "pool")
+    raises(lambda: mla.mla_append_cache(d, torch.zeros(3, 16, **bf), torch.zeros(D, 15, **bf),
+                                        torch.zeros(3, dtype=torch.int32), torch.zeros(3, dtype=torch.int32),
+                                        torch.zeros(2, 8, D, **bf), n_seqs=2, seq_stride=8), "w_dkv_kr")
+    raises(lambda: mla.mla_append_cache(d, torch.zeros(3, 16, **bf), torch.zeros(D, 16, **bf),
+                                        torch.zeros(2, dtype=torch.int32), torch.zeros(3, dtype=torch.int32),
+                                        torch.zeros(2, 8, D, **bf), n_seqs=2, seq_stride=8), "seq_idx")
+    raises(lambda: mla.mla_out_proj(d, torch.zeros(B, 4, 64, **bf), torch.zeros(4, 8, 64, **bf),
+                                    o_out=torch.zeros(B, 4, 7, **bf)), "o_out")
+    # right sizes get past the checks and stop at the device requirement
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mla.mla_out_proj(d, torch.zeros(B, 4, 64, **bf), torch.zeros(4, 8, 64, **bf))
