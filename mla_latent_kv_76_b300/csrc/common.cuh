@@ -10,6 +10,7 @@
 #include "../../include/mla.h"
 
 #define MLA_DEVI __device__ __forceinline__
+#define MLA_HD __host__ __device__ __forceinline__  // plain integer helpers, also checked on the host
 
 namespace mla {
 

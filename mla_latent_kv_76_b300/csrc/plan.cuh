@@ -34,12 +34,12 @@ MLA_DEVI int effective_len(const int32_t* seqlens, int b, int64_t capacity, int3
   return L;
 }
 
-MLA_DEVI int tiles_of(int L, int tile = kTileTokens) { return (L + tile - 1) / tile; }
+MLA_HD int tiles_of(int L, int tile = kTileTokens) { return (L + tile - 1) / tile; }
 
-MLA_DEVI int64_t worker_begin(int g, int64_t T, int G) { return (int64_t)g * T / G; }
+MLA_HD int64_t worker_begin(int g, int64_t T, int G) { return (int64_t)g * T / G; }
 
 // Largest g with worker_begin(g) <= x, i.e. the worker owning tile x.
-MLA_DEVI int worker_of(int64_t x, int64_t T, int G) {
+MLA_HD int worker_of(int64_t x, int64_t T, int G) {
   const int64_t g = ((x + 1) * (int64_t)G - 1) / T;
   return (int)(g < G - 1 ? g : G - 1);
 }
@@ -76,7 +76,7 @@ MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* s
 }
 
 // The sequence owning tile x: the largest b with pre[b] <= x.
-MLA_DEVI int seq_of_tile(const int* pre, int B, int64_t x) {
+MLA_HD int seq_of_tile(const int* pre, int B, int64_t x) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -95,15 +95,15 @@ MLA_DEVI int seq_of_tile(const int* pre, int B, int64_t x) {
 // two sequences when E <= G (each one writes a single partial, with no second
 // epilogue or query reload), and otherwise takes whole sequences.  Entry e's
 // partial lives in slot e.
-MLA_DEVI int plan_entries(int t, int64_t T, int n, int G) {
+MLA_HD int plan_entries(int t, int64_t T, int n, int G) {
   if (t <= 0) return 0;
   if (G <= n) return 1;
   const int64_t w = 1 + (int64_t)(G - n) * t / T;
   return (int)(w < t ? w : t);
 }
-MLA_DEVI int entry_start(int k, int t, int w) { return (int)((int64_t)t * k / w); }
+MLA_HD int entry_start(int k, int t, int w) { return (int)((int64_t)t * k / w); }
 // The entry (index within its sequence) holding tile tau of a sequence of t tiles.
-MLA_DEVI int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau + 1) * w - 1) / t); }
+MLA_HD int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau + 1) * w - 1) / t); }
 
 // Exclusive prefix of plan_entries over b into W[0..B] (shared memory), from the
 // tile prefix pre[0..B]; every thread of the block takes part and gets the same
@@ -116,6 +116,14 @@ MLA_DEVI int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau 
 // batches keep the aligned plan (16 x 4096: 8 vs 10); many ragged sequences take
 // the even split (64 sequences of 1024..8192 tokens: 64 vs 48).
 constexpr int kSegPenaltyTiles = 3;
+// The choice itself: cost_aligned = the aligned plan's longest entry (tiles),
+// T total tiles, G workers, t_min the shortest non-empty sequence's tiles.
+MLA_HD bool prefer_aligned(int cost_aligned, int64_t T, int G, int t_min) {
+  if (T == 0) return true;
+  const int64_t q = (T + G - 1) / G;
+  const int64_t cost_split = q + (int64_t)kSegPenaltyTiles * ((q + t_min - 1) / t_min);
+  return cost_aligned <= cost_split;
+}
 MLA_DEVI bool plan_prefix(const int* pre, int B, int G, int* W) {
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int per = (B + nthr - 1) / nthr;
@@ -182,17 +190,14 @@ MLA_DEVI bool plan_prefix(const int* pre, int B, int G, int* W) {
   }
   if (tid == nthr - 1) W[B] = run;
   __syncthreads();
-  if (T == 0) return true;
-  const int64_t q = (T + G - 1) / G;
-  const int64_t cost_split = q + (int64_t)kSegPenaltyTiles * ((q + s_tmin - 1) / s_tmin);
-  return cost_aligned <= cost_split;
+  return prefer_aligned(cost_aligned, T, G, s_tmin);
 }
 
 // The sequence owning entry e < W[B]: the largest b with W[b] <= e.
-MLA_DEVI int seq_of_entry(const int* W, int B, int64_t e) { return seq_of_tile(W, B, e); }
+MLA_HD int seq_of_entry(const int* W, int B, int64_t e) { return seq_of_tile(W, B, e); }
 
 // First global tile of entry e (T for e == E).
-MLA_DEVI int64_t entry_tile(const int* pre, const int* W, int B, int64_t e) {
+MLA_HD int64_t entry_tile(const int* pre, const int* W, int B, int64_t e) {
   if (e >= W[B]) return pre[B];
   const int b = seq_of_entry(W, B, e);
   const int t = pre[b + 1] - pre[b], w = W[b + 1] - W[b];

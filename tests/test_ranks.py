@@ -53,11 +53,12 @@ def test_two_gloo_ranks_agree_on_the_slowest_time(tmp_path):
         slowest = bench.max_over_ranks(mine, dist, "cpu")
         tokens = bench.job_tokens_per_s(16, world, slowest)
         dist.destroy_process_group()
-        print(json.dumps({"rank": rank, "mine": mine, "slowest": slowest, "tokens": tokens}), flush=True)
+        with open(os.path.join(sys.argv[1], f"rank{rank}.json"), "w") as f:
+            json.dump({"rank": rank, "mine": mine, "slowest": slowest, "tokens": tokens}, f)
     """))
-    r = _torchrun([str(script)], timeout=180)
+    r = _torchrun([str(script), str(tmp_path)], timeout=180)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    lines = [json.load(open(tmp_path / f"rank{i}.json")) for i in range(2)]
     assert sorted(d["rank"] for d in lines) == [0, 1]
     for d in lines:
         assert d["slowest"] == 57.5
