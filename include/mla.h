@@ -13,8 +13,9 @@
  * Conventions shared by every entry point
  *  - bf16 tensors are passed as void* holding __nv_bfloat16 values; all data
  *    pointers are DEVICE pointers owned by the caller.  The library allocates
- *    no device memory, keeps no state between calls and never synchronises
- *    the stream (except mla_read_status).
+ *    no device memory (mla_decode_attn_noalloc's static scratch aside), keeps
+ *    no state between calls beyond per-device launch attributes and never
+ *    synchronises the stream (except mla_read_status).
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *    enqueued asynchronously; the int return value is the result of host-side
  *    argument validation and of the launch itself.
@@ -78,7 +79,8 @@ typedef struct mla_dims {
  *   pos   [batch]             int32, position of the decode token
  *   w_uk  [n_h][d_h][d_c]     bf16 (k^C_i = W^UK_i c)
  *   q_out [batch][n_h][d_c + d_R] bf16
- * Requires d_h, d_c multiples of 8 and d_R even.  batch == 0 is a no-op.
+ * Requires d_h, d_c multiples of 8 and d_R even and <= 128
+ * (MLA_ERR_UNSUPPORTED otherwise).  batch == 0 is a no-op.
  */
 int mla_absorb_q(const mla_dims* dims, int32_t batch, const void* q_c, const void* q_r,
                  const int32_t* pos, const void* w_uk, void* q_out, void* stream);
@@ -96,7 +98,9 @@ int mla_absorb_q(const mla_dims* dims, int32_t batch, const void* q_c, const voi
  *   contiguous: block_table NULL, pool [n_seqs][seq_stride_tokens][D]
  * A token whose sequence, position or block id is out of range is skipped
  * and MLA_ERR_DEVICE_BOUNDS is stored in *dev_status.  Two tokens that map
- * to the same slot race.  Requires d_model a multiple of 8.
+ * to the same slot race.  Requires d_model and d_c + d_R multiples of 8, d_c
+ * even and d_R <= 128 (MLA_ERR_UNSUPPORTED otherwise).  n_tokens == 0 is a
+ * no-op.
  */
 int mla_append_cache(const mla_dims* dims, int32_t n_tokens, int32_t d_model, const void* h,
                      const void* w_dkv_kr, const int32_t* seq_idx, const int32_t* pos,
@@ -136,11 +140,17 @@ enum {
  *   scale    softmax scale, normally 1/sqrt(d_h + d_R)
  *   num_workers  split-KV workers (0 = automatic: one per SM pair on the
  *            tensor-core path); the result is the same for every value up to
- *            floating-point rounding.  The tensor-core path cuts sequence b
- *            into w_b = min(t_b, 1 + floor((G - n) t_b / T)) pieces (t_b its
- *            128-token tiles, T their sum, n non-empty sequences, G workers;
- *            one piece per sequence when G <= n), so no worker spans two
- *            sequences while the pieces fit the workers.
+ *            floating-point rounding.  The shape-generic path gives worker g
+ *            tiles [floor(g T / G), floor((g + 1) T / G)) of the batch's tile
+ *            list (T tiles, G workers).  The tensor-core path chooses, per
+ *            call and on the device, between that even split and cutting
+ *            sequence b into w_b = min(t_b, 1 + floor((G - n) t_b / T))
+ *            pieces (t_b its 128-token tiles, n non-empty sequences; one
+ *            piece per sequence when G <= n), which keeps each worker inside
+ *            one sequence while the pieces fit the workers; it takes the
+ *            pieces unless their longest exceeds the even split's bound
+ *            Q + 3 ceil(Q / t_min) (Q = ceil(T / G), t_min the fewest tiles
+ *            of a non-empty sequence).
  *   workspace / workspace_bytes: device scratch of at least
  *            mla_decode_workspace_size(dims, batch, num_workers) bytes; its
  *            contents on entry do not matter
@@ -198,7 +208,7 @@ int mla_decode_attn_noalloc(const mla_dims* dims, int32_t batch, const void* q, 
  *   z     [batch][n_h][d_c]  bf16
  *   w_uv  [n_h][d_v][d_c]    bf16
  *   o_out [batch][n_h][d_v]  bf16
- * Requires d_c a multiple of 8.
+ * Requires d_c and d_v multiples of 8 (MLA_ERR_UNSUPPORTED otherwise).
  */
 int mla_out_proj(const mla_dims* dims, int32_t batch, const void* z, const void* w_uv,
                  void* o_out, void* stream);
