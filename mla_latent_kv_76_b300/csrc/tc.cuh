@@ -24,15 +24,6 @@ MLA_DEVI void mbar_arrive(uint64_t* b) {
 MLA_DEVI void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
 }
-// Arrive on the barrier at the same offset in CTA `rank` of the cluster, with
-// release semantics at cluster scope (orders this thread's earlier stores,
-// including remote ones, before the arrival).
-MLA_DEVI void mbar_arrive_remote(uint64_t* local_b, uint32_t rank) {
-  uint32_t rb;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_b)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb) : "memory");
-}
-
 MLA_DEVI bool mbar_test(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -150,15 +141,6 @@ MLA_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
-MLA_DEVI void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets, descriptor version 1 (bit 46) and the swizzle mode in bits 61-63
 // (2 = 128-byte swizzle).
@@ -212,11 +194,6 @@ MLA_DEVI uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-MLA_DEVI uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
 MLA_DEVI void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -225,24 +202,9 @@ MLA_DEVI uint32_t map_peer(const void* local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
-MLA_DEVI void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-MLA_DEVI void st_cluster_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-MLA_DEVI void st_cluster_u32(uint32_t addr, uint32_t a) {
-  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
-}
-// Arrive on a barrier of another CTA given its shared::cluster address.
-MLA_DEVI void mbar_arrive_cluster_addr(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-// Same without release semantics: for a signal that orders none of this thread's
-// own memory operations (a cluster-scope release can stall the thread).
+// Arrive on a barrier of another CTA, given its shared::cluster address, without
+// release semantics: for a signal that orders none of this thread's own memory
+// operations (a cluster-scope release can stall the thread).
 MLA_DEVI void mbar_arrive_cluster_addr_relaxed(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
@@ -263,10 +225,5 @@ MLA_DEVI void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, u
                "r"(smem_u32(src)), "r"(bytes), "r"(dst_bar)
                : "memory");
 }
-// Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
-MLA_DEVI void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 }  // namespace tc
 }  // namespace mla
