@@ -10,7 +10,16 @@ import oracle as orc
 # max|d| <= 1e-2 * max|ref|  and  sum|d| / sum|ref| <= 2e-3  (mean relative error, L1 form)
 MAX_REL = 1e-2
 MEAN_REL = 2e-3
-LSE_ABS = 1e-3
+# lse: both decode kernels round the softmax weights p_j = 2^(x_j - m) to bf16 for
+# the value contraction and sum those same rounded weights into l, so that z is
+# an exact convex combination of the weights the MMA used.  bf16 keeps 8
+# significant bits: each weight carries a relative error of at most 2^-8, so
+# l does too and |d lse| <= ln(1 + 2^-8) (~3.9e-3; ~1e-3 typical on a 2-token
+# sequence, less on long ones where the errors average out).  The relative
+# 1e-3 |lse| term is the allowance for fp32 score accumulation (576-term dot
+# products, exp2 / log2) that held for every case at large |lse|.
+LSE_ABS = float(np.log1p(2.0 ** -8))
+LSE_REL = 1e-3
 
 
 def bits_to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -52,7 +61,7 @@ def assert_lse_close(got, ref, what="lse", tol=LSE_ABS):
     both_inf = np.isneginf(got) & np.isneginf(ref)
     with np.errstate(invalid="ignore"):
         d = np.where(both_inf, 0.0, np.abs(got - ref))
-    assert np.all(d <= tol * np.maximum(1.0, np.abs(np.where(both_inf, 0.0, ref)))), \
+    assert np.all(d <= tol + LSE_REL * np.abs(np.where(both_inf, 0.0, ref))), \
         f"{what}: max |d| = {np.nanmax(d):.3e}"
 
 

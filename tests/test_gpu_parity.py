@@ -469,3 +469,39 @@ def test_tc_out_of_range_inputs_are_reported_not_read(mla):
     bt[0, 0] = wl.num_blocks + 5
     z, lse, st = run_decode(mla, wl, block_table=i32(bt))
     assert st == 6 and np.isfinite(z).all()
+
+
+# ---------------------------------------------------------------- batch limits
+def _check_sampled(wl, z, lse, batches):
+    for b in batches:
+        L = int(wl.seqlens[b])
+        if L == 0:
+            assert np.all(z[b] == 0) and np.all(np.isneginf(lse[b]))
+            continue
+        rows = orc.gather_rows(wl.pool, b, L, wl.block_table, wl.block_tokens, wl.seq_stride)
+        z_ref, lse_ref = orc.decode_latent(orc.bf16_to_f64(wl.q[b]), rows, wl.scale, wl.d_latent)
+        assert_close(z[b], z_ref, f"z[{b}]")
+        assert_lse_close(lse[b], lse_ref)
+
+
+def test_tc_decode_at_its_batch_limit(mla):
+    """1024 sequences, the most the tensor-core decode takes (each CTA holds the
+    tile and plan prefixes of the whole batch in shared memory); ragged
+    1..129 tokens, contiguous cache; sampled sequences against the oracle."""
+    rng = np.random.default_rng(2100)
+    wl = mi.make_random(2100, 128, 512, 64, rng.integers(1, 130, size=1024), paged=False)
+    z, lse, st = run_decode(mla, wl)
+    assert st == 0 and np.isfinite(z).all()
+    _check_sampled(wl, z, lse, list(range(0, 1024, 41)) + [1023])
+
+
+def test_generic_decode_at_the_batch_limit(mla):
+    """4096 sequences (the largest batch mla_decode_attn accepts) on the
+    shape-generic path, with empty sequences among them, paged cache."""
+    rng = np.random.default_rng(2101)
+    wl = mi.make_random(2101, 16, 64, 16, rng.integers(0, 130, size=4096), paged=True)
+    assert (wl.seqlens == 0).any()
+    z, lse, st = run_decode(mla, wl)
+    assert st == 0
+    empty = np.flatnonzero(wl.seqlens == 0)[:8]
+    _check_sampled(wl, z, lse, sorted(set(list(range(0, 4096, 97)) + [4095] + list(empty))))
