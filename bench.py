@@ -429,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
     cpu = cpu_baseline(wl, args.cpu_seconds) if not args.no_cpu else None
     line = {
         "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(us_per_step / 1e3, 6), "higher_is_better": False,
+        "warmup": max(3, args.warmup), "ms_per_step": round(us_per_step / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), random-init weights)",
         "config": dict(workload_desc(wl), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
         "tokens_per_s": round(job_tokens_per_s(wl.batch, world, us_per_step), 1),
