@@ -300,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (lo < hi) tc::wait<false>(fb, m & 1, ab);  // no copy in flight at exit (fills: the query + m tiles)
+        if (lo < hi) tc::wait_drain<false>(fb, m & 1, ab);  // no copy in flight at exit (fills: the query + m tiles)
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -352,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         tc::mma_commit(&bars[kBarScDrained]);
-        tc::wait<false>(&bars[kBarScDrained], 0, ab);
+        tc::wait_drain<false>(&bars[kBarScDrained], 0, ab);
       }
     } else if (warp == 2 || warp == 3) {
       if (lane == 0) {
@@ -605,7 +605,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int k = 1; k <= kVStages && k <= hh; ++k) {  // no copy in flight at exit
           const int m = hh - k;
-          tc::wait<false>(&bars[kBarFull + m % kVStages], (m / kVStages) & 1, ab);
+          tc::wait_drain<false>(&bars[kBarFull + m % kVStages], (m / kVStages) & 1, ab);
         }
       }
     } else if (warp == 1) {
@@ -674,7 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         post(kEvtExit, 0, 0);
         tc::mma_commit(&bars[kBarVcDrained]);
-        tc::wait<false>(&bars[kBarVcDrained], 0, ab);
+        tc::wait_drain<false>(&bars[kBarVcDrained], 0, ab);
       }
     } else if (warp < 4) {
       // ------------------------------------------------------------ tail zeroing

@@ -71,6 +71,33 @@ MLA_DEVI bool wait(uint64_t* b, uint32_t parity, const Abort& ab) {
   }
 }
 
+// Wait for this CTA's own copies or MMAs in flight before it exits or frees
+// tensor memory.  Unlike `wait`, an abort raised by another role does not end
+// it at once: the work already issued still lands within microseconds, so it
+// keeps waiting, for at most ~50 ms once the abort flag is up (~2 s before).
+constexpr long long kDrainCycles = 100000000ll;
+
+template <bool kCluster>
+MLA_DEVI bool wait_drain(uint64_t* b, uint32_t parity, const Abort& ab) {
+  if (kCluster ? mbar_test_cluster(b, parity) : mbar_test(b, parity)) return true;
+  long long t0 = clock64();
+  bool aborted = false;
+  for (uint32_t it = 1;; ++it) {
+    if (kCluster ? mbar_test_cluster(b, parity) : mbar_test(b, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (!aborted && *ab.flag) {
+        aborted = true;
+        t0 = clock64();
+      }
+      if (clock64() - t0 > (aborted ? kDrainCycles : kWaitCycles)) {
+        *ab.flag = 1;
+        report(ab.status, MLA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 MLA_DEVI void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
   asm volatile(
