@@ -46,18 +46,19 @@ bool dims_basic_ok(const mla_dims* d) {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t off_o, off_lse, off_l, total;
+  size_t off_o, off_lse, off_l, off_lq, total;
 };
 
 // Workspace: per split-KV partial slot (worker g + sequence b) the latent
-// vector o [n_h][d_c] and two per-head scalars.
+// vector o [n_h][d_c] and three per-head scalars.
 WsLayout ws_layout(const mla_dims& d, int batch, int workers) {
   WsLayout w;
   const size_t slots = (size_t)workers + (size_t)batch;
   w.off_o = 256;
   w.off_lse = w.off_o + align256(slots * d.n_heads * d.d_latent * sizeof(float));
   w.off_l = w.off_lse + align256(slots * d.n_heads * sizeof(float));
-  w.total = w.off_l + align256(slots * d.n_heads * sizeof(float));
+  w.off_lq = w.off_l + align256(slots * d.n_heads * sizeof(float));
+  w.total = w.off_lq + align256(slots * d.n_heads * sizeof(float));
   return w;
 }
 
@@ -190,6 +191,7 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.plan_flag = static_cast<int32_t*>(workspace);  // first word of the 256-byte header
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse);
   a.l_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_l);
+  a.lq_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lq);
   a.z_out = z_out;
   a.z_is_fp32 = z_is_fp32 ? 1 : 0;
   a.lse_out = lse_out;

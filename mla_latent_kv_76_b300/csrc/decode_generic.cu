@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(NW * 32) decode_generic_kernel(const DecodeLau
   uint8_t* sP = smem + L.off_p;
   float* sMax = reinterpret_cast<float*>(smem + L.off_red);  // [NW][16]
   float* sSum = sMax + NW * kHG;                               // [NW][16]
+  float* sSumQ = sSum + NW * kHG;                              // [NW][16]
   constexpr int TPW = kTileTokens / NW;  // score tokens per warp
   constexpr int SB = TPW / 8;            // n8 blocks per warp in the score
   static_assert(SB == 1 || SB == 2, "4 or 8 warps");
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(NW * 32) decode_generic_kernel(const DecodeLau
     load_tile(0, 0);
     cp_async_commit();
 
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, lq_run[2] = {0.f, 0.f};
     constexpr int NB = DC / (8 * NW);  // n8 blocks of the latent per warp
     static_assert(NB >= 2 && NB % 2 == 0, "value columns are loaded two n8 blocks at a time");
     float o[NB][4];
@@ -195,8 +196,11 @@ __global__ void __launch_bounds__(NW * 32) decode_generic_kernel(const DecodeLau
         alpha[r] = exp2f(m_run[r] - mn);
         m_run[r] = mn;
         l_run[r] *= alpha[r];
+        lq_run[r] *= alpha[r];
       }
-      // ---- P = 2^(x - m), rounded to bf16 (the same weights feed the sum and l)
+      // ---- P = 2^(x - m), rounded to bf16 for the value MMA; l sums the fp32
+      // weights (for lse), lq the rounded ones (it normalises o, so o is an exact
+      // convex combination of the weights the MMA multiplied)
 #pragma unroll
       for (int nb = 0; nb < SB; ++nb)
 #pragma unroll
@@ -204,8 +208,8 @@ __global__ void __launch_bounds__(NW * 32) decode_generic_kernel(const DecodeLau
           const float p0 = exp2f(s[nb][2 * r] - m_run[r]);
           const float p1 = exp2f(s[nb][2 * r + 1] - m_run[r]);
           const uint32_t pk = pack_bf16x2(p0, p1);
-          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pk);
-          l_run[r] += __low2float(pb) + __high2float(pb);
+          l_run[r] += p0 + p1;
+          lq_run[r] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
           *reinterpret_cast<uint32_t*>(sP + (gq + 8 * r) * kPRow + (warp * TPW + nb * 8 + tq * 2) * 2) = pk;
         }
       __syncthreads();
@@ -239,21 +243,28 @@ __global__ void __launch_bounds__(NW * 32) decode_generic_kernel(const DecodeLau
     for (int r = 0; r < 2; ++r) {
       l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
       l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+      lq_run[r] += __shfl_xor_sync(0xffffffffu, lq_run[r], 1);
+      lq_run[r] += __shfl_xor_sync(0xffffffffu, lq_run[r], 2);
     }
     if (tq == 0) {
       sSum[warp * kHG + gq] = l_run[0];
       sSum[warp * kHG + gq + 8] = l_run[1];
+      sSumQ[warp * kHG + gq] = lq_run[0];
+      sSumQ[warp * kHG + gq + 8] = lq_run[1];
     }
     __syncthreads();
     const int64_t slot = (int64_t)wk + b;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int h = hg * kHG + gq + 8 * r;
-      float l = 0.f;
+      float l = 0.f, lq = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) l += sSum[w * kHG + gq + 8 * r];
+      for (int w = 0; w < NW; ++w) {
+        l += sSum[w * kHG + gq + 8 * r];
+        lq += sSumQ[w * kHG + gq + 8 * r];
+      }
       if (h >= a.n_heads) continue;
-      const float inv = 1.f / l;
+      const float inv = 1.f / lq;
       float* op = a.o_part + (slot * a.n_heads + h) * DC + warp * (DC / NW) + tq * 2;
 #pragma unroll
       for (int i = 0; i < NB; ++i)

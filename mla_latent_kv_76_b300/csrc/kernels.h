@@ -54,7 +54,8 @@ struct DecodeLaunch {
   int32_t workers;        // G
   float* o_part;          // [(G + B)][n_h][d_c]
   float* lse_part;        // [(G + B)][n_h]  generic: lse; tensor-core: reference maximum (log2)
-  float* l_part;          // [(G + B)][n_h]  tensor-core: weight sum relative to the maximum
+  float* l_part;          // [(G + B)][n_h]  tensor-core: fp32 weight sum relative to the maximum
+  float* lq_part;         // [(G + B)][n_h]  tensor-core: bf16-rounded weight sum relative to the maximum
   int32_t* plan_flag;     // tensor-core: which split plan the partial pass used (workspace header)
   void* z_out;
   int32_t z_is_fp32;

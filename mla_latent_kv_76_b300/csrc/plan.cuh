@@ -1,7 +1,7 @@
 // Split-KV work partition shared by the decode partial kernels and the combine.
 //
-// Even split (both decode paths): every sequence b is cut into tiles (64 tokens
-// on the shape-generic path, 128 on the tensor-core path); the tiles of all
+// Even split (both decode paths): every sequence b is cut into tiles of 64
+// tokens (one paged block); the tiles of all
 // sequences, in batch order, form one list of T tiles.  Worker g of G owns the
 // contiguous range [floor(g T / G), floor((g+1) T / G)), which may cover the end
 // of one sequence and the start of the next.  Each (worker, sequence) segment
@@ -36,24 +36,37 @@ MLA_DEVI int effective_len(const int32_t* seqlens, int b, int64_t capacity, int3
 
 MLA_HD int tiles_of(int L, int tile = kTileTokens) { return (L + tile - 1) / tile; }
 
-MLA_HD int64_t worker_begin(int g, int64_t T, int G) { return (int64_t)g * T / G; }
+// floor(n / d) for n >= 0, d > 0.  64-bit integer division is a long software
+// sequence on the GPU (it cost microseconds in the decode prologue), so the
+// common case where both fit in 32 bits takes the 32-bit instruction.
+MLA_HD int64_t div_floor(int64_t n, int64_t d) {
+  if ((uint64_t)n <= 0xFFFFFFFFull && (uint64_t)d <= 0xFFFFFFFFull) return (int64_t)((uint32_t)n / (uint32_t)d);
+  return n / d;
+}
+
+MLA_HD int64_t worker_begin(int g, int64_t T, int G) { return div_floor((int64_t)g * T, G); }
 
 // Largest g with worker_begin(g) <= x, i.e. the worker owning tile x.
 MLA_HD int worker_of(int64_t x, int64_t T, int G) {
-  const int64_t g = ((x + 1) * (int64_t)G - 1) / T;
+  const int64_t g = div_floor((x + 1) * (int64_t)G - 1, T);
   return (int)(g < G - 1 ? g : G - 1);
 }
 
 // Exclusive prefix of tiles_of(effective_len(b), tile) over b into pre[0..B]
 // (shared memory); every thread of the block takes part.  Invalid lengths
 // are reported once, by the thread that scans them.
+// When `lens` is given, the validated lengths are stored there too (shared memory).
 MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* status, int* pre,
-                          int tile = kTileTokens) {
+                          int tile = kTileTokens, int* lens = nullptr) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int per = (B + nthr - 1) / nthr;
   const int b0 = tid * per, b1 = min(B, b0 + per);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += tiles_of(effective_len(seqlens, b, cap, status), tile);
+  for (int b = b0; b < b1; ++b) {
+    const int L = effective_len(seqlens, b, cap, status);
+    if (lens) lens[b] = L;
+    local += tiles_of(L, tile);
+  }
   __shared__ int warp_sums[32];
   const int lane = tid & 31, warp = tid >> 5;
   int incl = local;
@@ -69,7 +82,7 @@ MLA_DEVI void tile_prefix(const int32_t* seqlens, int B, int64_t cap, int32_t* s
   int run = warp_off + incl - local;
   for (int b = b0; b < b1; ++b) {
     pre[b] = run;
-    run += tiles_of(effective_len(seqlens, b, cap, nullptr), tile);
+    run += tiles_of(lens ? lens[b] : effective_len(seqlens, b, cap, nullptr), tile);
   }
   if (tid == nthr - 1) pre[B] = run;  // the last thread's running sum is the total
   __syncthreads();
@@ -98,12 +111,12 @@ MLA_HD int seq_of_tile(const int* pre, int B, int64_t x) {
 MLA_HD int plan_entries(int t, int64_t T, int n, int G) {
   if (t <= 0) return 0;
   if (G <= n) return 1;
-  const int64_t w = 1 + (int64_t)(G - n) * t / T;
+  const int64_t w = 1 + div_floor((int64_t)(G - n) * t, T);
   return (int)(w < t ? w : t);
 }
-MLA_HD int entry_start(int k, int t, int w) { return (int)((int64_t)t * k / w); }
+MLA_HD int entry_start(int k, int t, int w) { return (int)div_floor((int64_t)t * k, w); }
 // The entry (index within its sequence) holding tile tau of a sequence of t tiles.
-MLA_HD int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau + 1) * w - 1) / t); }
+MLA_HD int entry_of_tile(int tau, int t, int w) { return (int)div_floor((int64_t)(tau + 1) * w - 1, t); }
 
 // Exclusive prefix of plan_entries over b into W[0..B] (shared memory), from the
 // tile prefix pre[0..B]; every thread of the block takes part and gets the same
@@ -112,16 +125,17 @@ MLA_HD int entry_of_tile(int tau, int t, int w) { return (int)(((int64_t)(tau + 
 // even split costs at most Q + kSegPenaltyTiles * ceil(Q / t_min) (Q = ceil(T/G)
 // tiles per worker, t_min the shortest non-empty sequence; a worker can meet at
 // most that many sequence boundaries, and each extra sequence costs one more
-// partial write and a query reload, ~kSegPenaltyTiles tile times).  Uniform
-// batches keep the aligned plan (16 x 4096: 8 vs 10); many ragged sequences take
-// the even split (64 sequences of 1024..8192 tokens: 64 vs 48).
-constexpr int kSegPenaltyTiles = 3;
+// partial write and a query reload, ~kSegPenaltyTiles 64-token tile times).  Uniform
+// batches keep the aligned plan (16 x 4096 over 74 workers: 16 vs 20 tiles of 64
+// tokens); many ragged sequences take the even split (64 sequences of
+// 1024..8192 tokens: 128 vs 87).
+constexpr int kSegPenaltyTiles = 6;
 // The choice itself: cost_aligned = the aligned plan's longest entry (tiles),
 // T total tiles, G workers, t_min the shortest non-empty sequence's tiles.
 MLA_HD bool prefer_aligned(int cost_aligned, int64_t T, int G, int t_min) {
   if (T == 0) return true;
-  const int64_t q = (T + G - 1) / G;
-  const int64_t cost_split = q + (int64_t)kSegPenaltyTiles * ((q + t_min - 1) / t_min);
+  const int64_t q = div_floor(T + G - 1, G);
+  const int64_t cost_split = q + (int64_t)kSegPenaltyTiles * div_floor(q + t_min - 1, t_min);
   return cost_aligned <= cost_split;
 }
 MLA_DEVI bool plan_prefix(const int* pre, int B, int G, int* W) {

@@ -7,18 +7,17 @@ import torch
 import oracle as orc
 
 # GPU vs oracle tolerance for floating-point outputs (bf16 storage, fp32 accumulation):
-# max|d| <= 1e-2 * max|ref|  and  sum|d| / sum|ref| <= 2e-3  (mean relative error, L1 form)
+#   max|d| <= 1e-2 * max|ref| on every output row (one (sequence, head) vector of the
+#   last axis), and sum|d| / sum|ref| <= 2e-3 (mean relative error, L1 form) on every
+#   sequence's output.  Batch-wide figures would let a long sequence's error hide
+#   behind a short sequence's larger magnitude.  The mean bound is not applied per
+#   row: the value contraction multiplies bf16-rounded softmax weights, and a row
+#   whose weight sits on two tokens carries a relative error of 0.5 |e1 - e2| with
+#   |e| up to 2^-8 (bf16 round-to-nearest), i.e. up to ~3.9e-3 on that row alone.
 MAX_REL = 1e-2
 MEAN_REL = 2e-3
-# lse: both decode kernels round the softmax weights p_j = 2^(x_j - m) to bf16 for
-# the value contraction and sum those same rounded weights into l, so that z is
-# an exact convex combination of the weights the MMA used.  bf16 keeps 8
-# significant bits: each weight carries a relative error of at most 2^-8, so
-# l does too and |d lse| <= ln(1 + 2^-8) (~3.9e-3; ~1e-3 typical on a 2-token
-# sequence, less on long ones where the errors average out).  The relative
-# 1e-3 |lse| term is the allowance for fp32 score accumulation (576-term dot
-# products, exp2 / log2) that held for every case at large |lse|.
-LSE_ABS = float(np.log1p(2.0 ** -8))
+# lse = log sum_j exp(s_j): the kernels sum the fp32 weights into it, so the only
+# errors are fp32 score accumulation and exp2 / log2 rounding.
 LSE_REL = 1e-3
 
 
@@ -37,6 +36,7 @@ def i32(a, device="cuda") -> torch.Tensor:
 
 
 def err_stats(got: np.ndarray, ref: np.ndarray):
+    """(max_rel, mean_rel) of the whole array, batch-wide."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     d = np.abs(got - ref)
@@ -45,24 +45,54 @@ def err_stats(got: np.ndarray, ref: np.ndarray):
     return float(max_rel), float(mean_rel)
 
 
+def row_stats(got: np.ndarray, ref: np.ndarray):
+    """Per-row (max_rel, mean_rel) arrays; a row is one vector of the last axis."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    g2 = got.reshape(-1, got.shape[-1])
+    r2 = ref.reshape(-1, ref.shape[-1])
+    d = np.abs(g2 - r2)
+    a = np.abs(r2)
+    max_rel = d.max(axis=1) / np.maximum(a.max(axis=1), 1e-300)
+    mean_rel = d.sum(axis=1) / np.maximum(a.sum(axis=1), 1e-300)
+    return max_rel, mean_rel
+
+
 def assert_close(got, ref, what: str, max_rel=MAX_REL, mean_rel=MEAN_REL):
+    """max bound on every row (last axis); mean bound on every sequence (the leading
+    axis of a [sequence, head, ...] array, or the whole array when it holds one
+    sequence's [head, ...] output)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
-    mx, mn = err_stats(got, ref)
-    assert mx <= max_rel and mn <= mean_rel, f"{what}: max_rel={mx:.3e} mean_rel={mn:.3e}"
-    return mx, mn
+    mx, _ = row_stats(got, ref)
+    units = got.shape[0] if got.ndim >= 3 else 1
+    d = np.abs(got - ref).reshape(units, -1)
+    a = np.abs(ref).reshape(units, -1)
+    mn = d.sum(axis=1) / np.maximum(a.sum(axis=1), 1e-300)
+    bad_rows, bad_units = mx > max_rel, mn > mean_rel
+    if bad_rows.any() or bad_units.any():
+        r = int(np.argmax(mx))
+        u = int(np.argmax(mn))
+        raise AssertionError(
+            f"{what}: {int(bad_rows.sum())} of {bad_rows.size} rows beyond the max bound "
+            f"(worst row {tuple(int(v) for v in np.unravel_index(r, got.shape[:-1]))}: max_rel={mx[r]:.3e}); "
+            f"{int(bad_units.sum())} of {units} sequences beyond the mean bound (worst sequence {u}: "
+            f"mean_rel={mn[u]:.3e})")
+    return float(mx.max()), float(mn.max())
 
 
-def assert_lse_close(got, ref, what="lse", tol=LSE_ABS):
+def assert_lse_close(got, ref, what="lse", rel=LSE_REL):
+    """|d lse| <= rel * max(1, |lse|) elementwise; -inf (empty sequence) must match."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     both_inf = np.isneginf(got) & np.isneginf(ref)
     with np.errstate(invalid="ignore"):
         d = np.where(both_inf, 0.0, np.abs(got - ref))
-    assert np.all(d <= tol + LSE_REL * np.abs(np.where(both_inf, 0.0, ref))), \
-        f"{what}: max |d| = {np.nanmax(d):.3e}"
+    bound = rel * np.maximum(1.0, np.abs(np.where(both_inf, 0.0, ref)))
+    ok = d <= bound
+    assert ok.all(), f"{what}: {int((~ok).sum())} values beyond 1e-3 max(1,|lse|); max |d| = {np.nanmax(d):.3e}"
 
 
 def ulp_diff_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import mla_inputs as mi
-from helpers import assert_close, assert_lse_close, bits_to_dev, i32
+from helpers import bits_to_dev, i32
 
 pytestmark = pytest.mark.gpu
 
@@ -49,9 +49,9 @@ def test_noalloc_matches_regular_decode_on_two_calls_in_a_row(mla):
                                     dev_status=status, **kw)
         torch.cuda.synchronize()
         assert mla.mla_read_status(status) == 0
-        zr, zg = z_ref.cpu().numpy(), z.cpu().numpy()
-        assert_close(zg, zr, "z noalloc vs regular")
-        assert_lse_close(lse.cpu().numpy(), lse_ref.cpu().numpy())
+        # the same kernels, split plan and inputs: the results are bit for bit equal
+        assert torch.equal(z.view(torch.int32), z_ref.view(torch.int32)), "z noalloc vs regular"
+        assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32)), "lse noalloc vs regular"
 
 
 def test_noalloc_second_call_allocates_nothing(mla):
@@ -68,7 +68,7 @@ def test_noalloc_second_call_allocates_nothing(mla):
     mla.mla_decode_attn_noalloc(dims, a["q"], a["pool"], a["seqlens"], wl.scale, z_out=z, lse_out=lse, **kw)
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free_before
-    assert_close(z.cpu().numpy(), first.cpu().numpy(), "z second call")
+    assert torch.equal(z.view(torch.int32), first.view(torch.int32)), "z second call"
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(mla):
