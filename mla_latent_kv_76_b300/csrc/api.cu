@@ -49,8 +49,8 @@ struct WsLayout {
   size_t off_o, off_lse, off_l, off_lq, total;
 };
 
-// Workspace: per split-KV partial slot (worker g + sequence b) the latent
-// vector o [n_h][d_c] and three per-head scalars.
+// Workspace: a 256-byte header, then per split-KV partial slot (worker g +
+// sequence b) the latent vector o [n_h][d_c] and three per-head scalars.
 WsLayout ws_layout(const mla_dims& d, int batch, int workers) {
   WsLayout w;
   const size_t slots = (size_t)workers + (size_t)batch;

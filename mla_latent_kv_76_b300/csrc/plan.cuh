@@ -1,7 +1,7 @@
 // Split-KV work partition shared by the decode partial kernels and the combine.
 //
-// Even split (both decode paths): every sequence b is cut into tiles of 64
-// tokens (one paged block); the tiles of all
+// Even split (both decode paths): every sequence b is cut into tiles (64 tokens
+// on the shape-generic path, 128 on the tensor-core path); the tiles of all
 // sequences, in batch order, form one list of T tiles.  Worker g of G owns the
 // contiguous range [floor(g T / G), floor((g+1) T / G)), which may cover the end
 // of one sequence and the start of the next.  Each (worker, sequence) segment
@@ -125,11 +125,11 @@ MLA_HD int entry_of_tile(int tau, int t, int w) { return (int)div_floor((int64_t
 // even split costs at most Q + kSegPenaltyTiles * ceil(Q / t_min) (Q = ceil(T/G)
 // tiles per worker, t_min the shortest non-empty sequence; a worker can meet at
 // most that many sequence boundaries, and each extra sequence costs one more
-// partial write and a query reload, ~kSegPenaltyTiles 64-token tile times).  Uniform
-// batches keep the aligned plan (16 x 4096 over 74 workers: 16 vs 20 tiles of 64
-// tokens); many ragged sequences take the even split (64 sequences of
-// 1024..8192 tokens: 128 vs 87).
-constexpr int kSegPenaltyTiles = 6;
+// partial write and a query reload, ~kSegPenaltyTiles 128-token tile times).
+// Uniform batches keep the aligned plan (16 x 4096 over 74 workers: 8 vs 10);
+// many ragged sequences take the even split (64 sequences of 1024..8192
+// tokens: 64 vs 48).
+constexpr int kSegPenaltyTiles = 3;
 // The choice itself: cost_aligned = the aligned plan's longest entry (tiles),
 // T total tiles, G workers, t_min the shortest non-empty sequence's tiles.
 MLA_HD bool prefer_aligned(int cost_aligned, int64_t T, int G, int t_min) {

@@ -106,17 +106,6 @@ MLA_DEVI void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
-// 4-D tiled load.  The decode views a cache (or query) tensor as
-// [rows][9 column chunks of 64][...] with the chunk dimension ordered outside
-// the row dimension, so one copy lands several 64-column chunks, each as its
-// own 128-byte-swizzled [rows][128 B] tile.
-MLA_DEVI void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
-      : "memory");
-}
 MLA_DEVI void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -262,30 +251,6 @@ MLA_DEVI void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, u
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "r"(smem_u32(src)), "r"(bytes), "r"(dst_bar)
                : "memory");
-}
-// Arrive once on a barrier of another CTA (shared::cluster address) and add
-// `bytes` to its expected transactions; relaxed, like the arrive above.
-MLA_DEVI void mbar_expect_tx_remote(uint32_t remote_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(remote_bar),
-               "r"(bytes)
-               : "memory");
-}
-// Asynchronous stores into another CTA's shared memory (shared::cluster
-// address); each completes `bytes` transactions on the destination barrier.
-MLA_DEVI void st_async_v4(uint32_t dst, const uint4& v, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
-               : "memory");
-}
-MLA_DEVI void st_async_b32(uint32_t dst, uint32_t v, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst), "r"(v),
-               "r"(remote_bar)
-               : "memory");
-}
-// Add 1 to a counter in another CTA's shared memory (a progress signal that
-// orders nothing).
-MLA_DEVI void red_add_remote(uint32_t remote_addr, uint32_t v) {
-  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(remote_addr), "r"(v) : "memory");
 }
 }  // namespace tc
 }  // namespace mla

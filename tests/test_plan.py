@@ -19,7 +19,7 @@ import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SEG_PENALTY_TILES = 6
+SEG_PENALTY_TILES = 3
 
 
 @pytest.fixture(scope="module")
@@ -147,8 +147,8 @@ def check_case(G, tile, L, res):
 
 
 EDGE_CASES = [
-    (74, 64, [4096] * 16),                  # DeepSeek-V3 batch: aligned, 16 vs 20 tile-times
-    (74, 64, [131072] * 4),                 # long context: aligned, 114 vs 117
+    (74, 128, [4096] * 16),                 # DeepSeek-V3 batch: aligned, 8 vs 10 tile-times
+    (74, 128, [131072] * 4),                # long context: aligned, 57 vs 59
     (74, 128, [0, 0, 0, 0, 0]),             # nothing to do
     (74, 128, [131072]),                    # one sequence over every worker
     (1, 64, [300, 5, 0, 77]),               # one worker
@@ -163,8 +163,8 @@ EDGE_CASES = [
 
 def test_documented_plan_choices(harness):
     res = run_cases(harness, EDGE_CASES[:2])
-    assert res[0]["aligned"] == 1 and res[0]["cost"] == 16 and res[0]["W"][-1] == 64
-    assert res[1]["aligned"] == 1 and res[1]["cost"] == 114
+    assert res[0]["aligned"] == 1 and res[0]["cost"] == 8 and res[0]["W"][-1] == 64
+    assert res[1]["aligned"] == 1 and res[1]["cost"] == 57
 
 
 def test_edge_cases(harness):
@@ -198,6 +198,6 @@ def test_plan_choice_flips_for_many_ragged_sequences(harness):
     longest entry exceeds the split's bound); the checks still hold."""
     rng = np.random.default_rng(7)
     L = [int(v) for v in rng.integers(1024, 8193, size=64)]
-    (res,) = run_cases(harness, [(74, 64, L)])
-    check_case(74, 64, L, res)
+    (res,) = run_cases(harness, [(74, 128, L)])
+    check_case(74, 128, L, res)
     assert res["aligned"] == 0
