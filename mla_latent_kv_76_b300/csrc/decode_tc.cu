@@ -88,13 +88,12 @@ constexpr int kOffP = kOffStage + kVStages * kVStageBytes;  // [4] P hand-off bu
 constexpr int kOffBar = (kOffLsum + 2 * kH * 4 > kOffP + kPBufs * kPBufBytes) ? kOffLsum + 2 * kH * 4
                                                                              : kOffP + kPBufs * kPBufBytes;
 constexpr int kNumBars = 40;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, event descriptor
-constexpr int kOffPrefix = kOffMisc + 32;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, event descriptor, plan scalars
+constexpr int kOffPrefix = kOffMisc + 64;          // lens[B], pre[B + 1], W[B + 1]
 
 // score CTA barriers
 constexpr int kBarCfull = 0, kBarCempty = 3, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
-              kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35,
-              kBarQringFree = 37;
+              kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35, kBarQrope = 37;
 // value CTA barriers
 constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOcomp = 14, kBarEvt = 15,
               kBarEvtdone = 16, kBarVcDrained = 17;
@@ -106,7 +105,8 @@ constexpr uint32_t kColS = 0, kColQ = 256;
 
 enum { kEvtRescale = 1, kEvtEpilogue = 2, kEvtExit = 3 };
 
-size_t tc_smem_bytes(int batch) { return (size_t)kOffPrefix + 2 * (size_t)(batch + 1) * 4 + 1024; }
+size_t tc_smem_bytes(int batch) { return (size_t)kOffPrefix + (3 * (size_t)batch + 2) * 4 + 1024; }
+static_assert(kOffPrefix + (3 * kTcMaxBatch + 2) * 4 + 1024 <= 227 * 1024, "shared memory of one CTA");
 
 struct TcParams {
   const __nv_bfloat16* q;
@@ -132,13 +132,13 @@ struct Seg {
   int b, t_begin, ntile, len;
 };
 
-MLA_DEVI Seg seg_at(const int* pre, int B, int64_t x, int64_t hi, const TcParams& p, int64_t cap) {
+MLA_DEVI Seg seg_at(const int* pre, const int* lens, int B, int64_t x, int64_t hi) {
   Seg s;
   s.b = seq_of_tile(pre, B, x);
   s.t_begin = (int)(x - pre[s.b]);
   const int64_t e = pre[s.b + 1] < hi ? pre[s.b + 1] : hi;
   s.ntile = (int)(e - x);
-  s.len = effective_len(p.seqlens, s.b, cap, nullptr);
+  s.len = lens[s.b];
   return s;
 }
 
@@ -160,27 +160,50 @@ MLA_DEVI int half_block(const TcParams& p, const Seg& s, int tt, int w) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map, const __grid_constant__ CUtensorMap cache_map128,
-                     const __grid_constant__ CUtensorMap q_map, const TcParams p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_v,
+                     const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap q_map3,
+                     const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(sm + kOffMisc + 4);
   volatile int* evt_desc = reinterpret_cast<volatile int*>(sm + kOffMisc + 8);  // type, buffer, slot
-  int* pre = reinterpret_cast<int*>(sm + kOffPrefix);
+  int64_t* range = reinterpret_cast<int64_t*>(sm + kOffMisc + 32);                // this worker's [lo, hi)
+  int* aligned_s = reinterpret_cast<int*>(sm + kOffMisc + 48);
+  int* lens = reinterpret_cast<int*>(sm + kOffPrefix);
+  int* pre = lens + p.batch;
+  int* Wp = pre + p.batch + 1;  // entries prefix of the split plan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = tc::cluster_rank();
   const int g = (int)(blockIdx.x >> 1);
   const int64_t cap = p.paged ? (int64_t)p.max_blocks * 64 : p.seq_stride;
 
-  if (tid == 0) {
+  // Prologue, three warps in parallel: warp 0 builds the split plan (lengths,
+  // tile and entry prefixes, this worker's tile range), warp 1 allocates tensor
+  // memory, warp 2 initialises the barriers.
+  if (warp == 0) {
+    const bool al = warp_plan(p.seqlens, p.batch, cap, p.status, p.workers, kTile, lens, pre, Wp);
+    if (lane == 0) {
+      const int B = p.batch, G = p.workers;
+      const int64_t E = Wp[B], T = pre[B];
+      // worker g's contiguous run of tiles: entries [g E / G, (g + 1) E / G) of the
+      // sequence-aligned plan, or the even split [g T / G, (g + 1) T / G)
+      range[0] = al ? entry_tile(pre, Wp, B, div_floor((int64_t)g * E, G)) : worker_begin(g, T, G);
+      range[1] = al ? entry_tile(pre, Wp, B, div_floor((int64_t)(g + 1) * E, G)) : worker_begin(g + 1, T, G);
+      *aligned_s = al ? 1 : 0;
+      if (blockIdx.x == 0) *p.plan_flag = al ? 1 : 0;
+    }
+  } else if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 512);
+  } else if (tid == 64) {
     if (rank == 0) {
       for (int i = 0; i < kSlots; ++i) {
-        tc::mbar_init(&bars[kBarCfull + i], 3);  // one arrival per issuing lane
+        tc::mbar_init(&bars[kBarCfull + i], 1);  // the producer's expect_tx (+ the copies' bytes)
         tc::mbar_init(&bars[kBarCempty + i], 1);
       }
+      tc::mbar_init(&bars[kBarQrope], 1);
       for (int i = 0; i < 2; ++i) {
         tc::mbar_init(&bars[kBarSfull + i], 1);
         tc::mbar_init(&bars[kBarSfree + i], 256);
@@ -193,10 +216,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[kBarXmax], 256);
       tc::mbar_init(&bars[kBarXmax + 1], 256);
       tc::mbar_init(&bars[kBarLsum], 256);
-      tc::mbar_init(&bars[kBarQringFree], 256);
     } else {
       for (int i = 0; i < kVStages; ++i) {
-        tc::mbar_init(&bars[kBarFull + i], 8);  // one arrival per issuing lane
+        tc::mbar_init(&bars[kBarFull + i], 1);  // the producer's expect_tx (+ the copy's bytes)
         tc::mbar_init(&bars[kBarEmpty + i], 1 + 64);
         tc::mbar_init(&bars[kBarFix + i], 64);
       }
@@ -211,23 +233,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
-  tile_prefix(p.seqlens, p.batch, cap, p.status, pre, kTile);  // ends with __syncthreads
-  int* Wp = pre + p.batch + 1;                                  // entries prefix of the split plan
-  const bool aligned = plan_prefix(pre, p.batch, p.workers, Wp);  // ends with __syncthreads
-  if (blockIdx.x == 0 && tid == 0) *p.plan_flag = aligned ? 1 : 0;
   tc::tc_fence_before();
-  tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival
+  tc::cluster_sync();  // the plan and both CTAs' barriers are visible before any use or remote arrival
   tc::tc_fence_after();
   const uint32_t tb = *tmem_slot;
   const tc::Abort ab{abort_flag, p.status};
 
-  const int B = p.batch, G = p.workers;
-  // worker g's contiguous run of tiles: entries [g E / G, (g + 1) E / G) of the
-  // sequence-aligned plan, or the even split [g T / G, (g + 1) T / G)
-  const int64_t E = Wp[B], T = pre[B];
-  const int64_t lo = aligned ? entry_tile(pre, Wp, B, (int64_t)g * E / G) : worker_begin(g, T, G);
-  const int64_t hi = aligned ? entry_tile(pre, Wp, B, (int64_t)(g + 1) * E / G) : worker_begin(g + 1, T, G);
+  const int B = p.batch;
+  const int64_t lo = range[0], hi = range[1];
+  const bool aligned = *aligned_s != 0;
   // the partial slot of a segment: the plan entry it starts with, or worker + sequence
   auto slot_of = [&](const Seg& s) -> int64_t {
     if (!aligned) return (int64_t)g + s.b;
@@ -238,73 +252,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (rank == 0) {
     // ================================================================ score CTA
     if (warp == 0) {
-      if (lane < 3 * kSlots) {
-        // ---------------------------------------------------------- TMA producer, lane c = column chunk c
-        // (ring slot c / 3).  One issuing thread keeps only one or two copies moving,
-        // so every chunk of a tile has its own issuing lane.
-        const int c = lane, t = c / 3;
-        if (c == 0) {
-          tc::prefetch_map(&cache_map);
-          tc::prefetch_map(&cache_map128);
-        }
-        uint8_t* dst = sm + kOffRing + t * kSlotBytes + (c % 3) * kChunk128;
-        uint64_t* fb = &bars[kBarCfull + t];
+      if (lane == 0) {
+        // ---------------------------------------------------------- TMA producer (one thread)
+        // A copy costs the SM's TMA unit a roughly fixed time up to ~24 KB
+        // (measured on B300: ~2.6 copies/us per SM), so on the contiguous cache a
+        // ring slot (three 64-column chunks of 128 tokens) is one 48 KB 4-D box.
+        // On the paged cache a chunk's two 64-token halves come from two blocks
+        // at unrelated addresses and must land 8 KB apart, so a slot takes six
+        // 8 KB boxes.  Copies from divergent lanes of one warp were slower still
+        // than from one thread.
+        tc::prefetch_map(&map_s);
         bool ok = true;
-        int m = 0;  // tiles loaded so far
-        // The first segment's query (128 heads x 576 = exactly the three ring
-        // slots, same 128-byte-swizzled layout) comes through the ring ahead of
-        // tile 0: as per-thread loads it took ~7 us to arrive and held back the
-        // tile copies.  The softmax warps move it to TMEM and free the ring.
+        int m = 0;                      // tiles loaded so far
+        int fills[kSlots] = {0, 0, 0};  // fills issued per slot (for the exit drain)
+        // Fill 0 of the ring is the first segment's query (128 heads x 576, the
+        // same 128-byte-swizzled chunk layout): chunks 0-7 into the three slots
+        // for the MMA thread to copy into tensor memory (which frees each slot
+        // for tile 0), the RoPE chunk (8) straight to its own buffer.
         if (lo < hi) {
-          tc::prefetch_map(&q_map);
-          tc::mbar_expect_tx(fb, kChunk128);
-          tc::tma_load_3d(dst, &q_map, c * 64, 0, seq_of_tile(pre, B, lo), fb);
-          ok = tc::wait<false>(&bars[kBarQringFree], 0, ab);
+          const int b0 = seq_of_tile(pre, B, lo);
+          tc::mbar_expect_tx(&bars[kBarCfull + 0], 3 * kChunk128);
+          tc::tma_load_4d(sm + kOffRing, &q_map, 0, 0, 0, b0, &bars[kBarCfull + 0]);
+          tc::mbar_expect_tx(&bars[kBarCfull + 1], 3 * kChunk128);
+          tc::tma_load_4d(sm + kOffRing + kSlotBytes, &q_map, 0, 0, 3, b0, &bars[kBarCfull + 1]);
+          tc::mbar_expect_tx(&bars[kBarCfull + 2], 2 * kChunk128);
+          tc::tma_load_3d(sm + kOffRing + 2 * kSlotBytes, &q_map3, 6 * 64, 0, b0, &bars[kBarCfull + 2]);
+          tc::tma_load_3d(sm + kOffRing + 2 * kSlotBytes + kChunk128, &q_map3, 7 * 64, 0, b0, &bars[kBarCfull + 2]);
+          tc::mbar_expect_tx(&bars[kBarQrope], kChunk128);
+          tc::tma_load_3d(sm + kOffQrope, &q_map3, 8 * 64, 0, b0, &bars[kBarQrope]);
+          for (int t = 0; t < kSlots; ++t) fills[t] = 1;
         }
         for (int64_t x = lo; x < hi && ok;) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          const Seg s = seg_at(pre, lens, B, x, hi);
           x += s.ntile;
           // the next segment's query (147 KB) is warmed in L2 a whole segment ahead
-          if (c == 0 && x < hi)
-            tc::prefetch_l2(p.q + (int64_t)seq_of_tile(pre, B, x) * kH * kD, (uint32_t)(kH * kD * 2));
-          for (int j = 0; j < s.ntile; ++j, ++m) {
+          if (x < hi) tc::prefetch_l2(p.q + (int64_t)seq_of_tile(pre, B, x) * kH * kD, (uint32_t)(kH * kD * 2));
+          for (int j = 0; j < s.ntile && ok; ++j, ++m) {
             const int tt = s.t_begin + j;
-            if (m >= 1 && !tc::wait<false>(&bars[kBarCempty + t], (m - 1) & 1, ab)) {
-              ok = false;
-              break;
+            const int nh = p.paged ? halves_of(s, tt) : 0;
+            int blk[2] = {-1, -1};
+            for (int w = 0; w < nh; ++w) {
+              blk[w] = half_block(p, s, tt, w);
+              if (blk[w] < 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
             }
-            if (p.paged) {
-              const int nh = halves_of(s, tt);
-              int blk[2] = {-1, -1};
-              int nvalid = 0;
-              for (int w = 0; w < nh; ++w) {
-                blk[w] = half_block(p, s, tt, w);
-                if (blk[w] < 0) {
-                  if (c == 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
-                  // unreadable block: its rows count as zeros
-                  uint4* z = reinterpret_cast<uint4*>(dst + w * kChunkBytes);
-                  for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
-                } else {
-                  ++nvalid;
+#pragma unroll 1
+            for (int t = 0; t < kSlots; ++t) {
+              if (!tc::wait<false>(&bars[kBarCempty + t], m & 1, ab)) {  // fill m (0: the query) consumed
+                ok = false;
+                break;
+              }
+              uint8_t* dst = sm + kOffRing + t * kSlotBytes;
+              uint64_t* fb = &bars[kBarCfull + t];
+              ++fills[t];
+              if (p.paged) {
+                // chunk 3t + cc of block w (the tile's 64-token half w) at dst + cc * 16 KB + w * 8 KB
+                int nvalid = 0;
+                for (int w = 0; w < nh; ++w) {
+                  if (blk[w] >= 0) {
+                    ++nvalid;
+                  } else {  // unreadable block: its rows count as zeros
+                    for (int cc = 0; cc < 3; ++cc) {
+                      uint4* z = reinterpret_cast<uint4*>(dst + cc * kChunk128 + w * kChunkBytes);
+                      for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                    }
+                  }
                 }
+                if (nvalid < nh) tc::fence_async_smem();
+                if (nvalid == 0) {
+                  tc::mbar_arrive(fb);
+                  continue;
+                }
+                tc::mbar_expect_tx(fb, nvalid * 3 * kChunkBytes);
+                for (int cc = 0; cc < 3; ++cc)
+                  for (int w = 0; w < nh; ++w)
+                    if (blk[w] >= 0)
+                      tc::tma_load_4d(dst + cc * kChunk128 + w * kChunkBytes, &map_s, 0, 0, 3 * t + cc, blk[w], fb);
+              } else {
+                // contiguous cache: 128 tokens x chunks 3t .. 3t + 2, chunk-major (rows
+                // past the sequence are masked by the softmax; past the allocation they
+                // read as zero)
+                tc::mbar_expect_tx(fb, kSlotBytes);
+                tc::tma_load_4d(dst, &map_s, 0, tt * kTile, 3 * t, s.b, fb);
               }
-              if (nvalid < nh) tc::fence_async_smem();
-              if (nvalid == 0) {
-                tc::mbar_arrive(fb);
-                continue;
-              }
-              tc::mbar_expect_tx(fb, nvalid * kChunkBytes);
-              for (int w = 0; w < nh; ++w)
-                if (blk[w] >= 0) tc::tma_load_3d(dst + w * kChunkBytes, &cache_map, c * 64, 0, blk[w], fb);
-            } else {
-              // contiguous cache: one 128-row box per 64-column chunk (rows past the
-              // sequence are masked by the softmax; past the allocation they read as zero)
-              tc::mbar_expect_tx(fb, kChunk128);
-              tc::tma_load_3d(dst, &cache_map128, c * 64, tt * kTile, s.b, fb);
             }
           }
         }
-        if (lo < hi) tc::wait_drain<false>(fb, m & 1, ab);  // no copy in flight at exit (fills: the query + m tiles)
+        // no copy in flight at exit: the last fill of every slot has landed
+        for (int t = 0; t < kSlots; ++t)
+          if (fills[t] > 0) tc::wait_drain<false>(&bars[kBarCfull + t], (fills[t] - 1) & 1, ab);
+        if (lo < hi) tc::wait_drain<false>(&bars[kBarQrope], 0, ab);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -315,9 +351,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int m = 0, k = 0;
         bool ok = true;
         for (int64_t x = lo; x < hi && ok; ++k) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          const Seg s = seg_at(pre, lens, B, x, hi);
           x += s.ntile;
-          if (!tc::wait<false>(&bars[kBarQready], k & 1, ab)) break;
+          if (k == 0) {
+            // the first segment's query, ring fill 0: latent chunks 0-7 into tensor
+            // memory (the copies run ahead of the MMAs issued below), then each
+            // slot goes back to the producer; the RoPE chunk is read in place
+#pragma unroll
+            for (int t = 0; t < kSlots; ++t) {
+              if (!tc::wait<false>(&bars[kBarCfull + t], 0, ab)) {
+                ok = false;
+                break;
+              }
+              tc::tc_fence_after();
+#pragma unroll
+              for (int cc = 0; cc < 3; ++cc) {
+                const int c = 3 * t + cc;
+                if (c < 8)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    tc::tmem_cp_128x256b(tb + kColQ + c * 32 + kk * 8,
+                                         tc::smem_desc(ring + t * kSlotBytes + cc * kChunk128 + kk * 32, 16, 1024));
+              }
+              tc::mma_commit(&bars[kBarCempty + t]);
+            }
+            if (!ok || !tc::wait<false>(&bars[kBarQrope], 0, ab)) break;
+          } else if (!tc::wait<false>(&bars[kBarQready], (k - 1) & 1, ab)) {  // a later segment's query
+            break;
+          }
           for (int j = 0; j < s.ntile && ok; ++j, ++m) {
             // S is double-buffered: buffer m & 1 is free once the softmax read tile m - 2
             if (m >= 2 && !tc::wait<false>(&bars[kBarSfree + (m & 1)], ((m >> 1) - 1) & 1, ab)) {
@@ -334,20 +395,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
               }
               tc::tc_fence_after();
+              {
+                // chunk c of the slot: 128 tokens x 64 columns, N = 128
 #pragma unroll
-              for (int cc = 0; cc < 3; ++cc) {
-                const int c = 3 * t + cc;
-                const uint32_t sa = ring + t * kSlotBytes + cc * kChunk128;
-                if (c < 8) {
+                for (int cc = 0; cc < 3; ++cc) {
+                  const int c = 3 * t + cc;
+                  const uint32_t sa = ring + t * kSlotBytes + cc * kChunk128;
+                  if (c < 8) {
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_ts(dS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
-                               (c | kk) != 0 ? 1u : 0u);
-                } else {
+                    for (int kk = 0; kk < 4; ++kk)
+                      tc::mma_ts(dS, tb + kColQ + c * 32 + kk * 8, tc::smem_desc(sa + kk * 32, 16, 1024), idS,
+                                 (c | kk) != 0 ? 1u : 0u);
+                  } else {
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_ss(dS, tc::smem_desc(qrope + kk * 32, 16, 1024), tc::smem_desc(sa + kk * 32, 16, 1024),
-                               idS, 1u);
+                    for (int kk = 0; kk < 4; ++kk)
+                      tc::mma_ss(dS, tc::smem_desc(qrope + kk * 32, 16, 1024), tc::smem_desc(sa + kk * 32, 16, 1024),
+                                 idS, 1u);
+                  }
                 }
               }
               tc::mma_commit(&bars[kBarCempty + t]);
@@ -368,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int hh = 0, u = 0;
         bool ok = true;
         for (int64_t x = lo; x < hi && ok;) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          const Seg s = seg_at(pre, lens, B, x, hi);
           x += s.ntile;
           for (int j = 0; j < s.ntile && ok; ++j) {
             const int nh = halves_of(s, s.t_begin + j);
@@ -434,50 +498,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars[kBarQready]);
       };
 
-      // the first segment's query, TMA-loaded into the three ring slots: latent
-      // chunks 4 w .. 4 w + 3 of row h to TMEM, the RoPE chunk (8) to kOffQrope
-      // (same swizzled layout, so a straight copy), then the ring goes back to the
-      // producer
-      auto q_from_ring = [&]() -> bool {
-        for (int t = 0; t < kSlots; ++t)
-          if (!tc::wait<false>(&bars[kBarCfull + t], 0, ab)) return false;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = 4 * w + cc;
-          const uint8_t* row = sm + kOffRing + (c / 3) * kSlotBytes + (c % 3) * kChunk128 + h * 128;
-          uint32_t r[32];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row + ((j ^ (h & 7)) * 16));
-            r[4 * j] = v.x;
-            r[4 * j + 1] = v.y;
-            r[4 * j + 2] = v.z;
-            r[4 * j + 3] = v.w;
-          }
-          tc::tmem_st32(lane_t + kColQ + 128 * w + 32 * cc, r);
-        }
-        const uint8_t* rope = sm + kOffRing + 2 * kSlotBytes + 2 * kChunk128 + h * 128 + 64 * w;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(sm + kOffQrope + h * 128 + 64 * w + 16 * j) =
-              *reinterpret_cast<const uint4*>(rope + 16 * j);
-        tc::fence_async_smem();
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars[kBarQready]);
-        tc::mbar_arrive(&bars[kBarQringFree]);
-        return true;
-      };
-
       int m = 0, hh = 0, k = 0;
-      bool ok = true, first = true;
+      bool ok = true;
       for (int64_t x = lo; x < hi && ok; ++k) {
-        const Seg s = seg_at(pre, B, x, hi, p, cap);
+        const Seg s = seg_at(pre, lens, B, x, hi);
         x += s.ntile;
-        if (first) {
-          if (!q_from_ring()) break;
-        }
-        first = false;
         float m_ref = -INFINITY, l = 0.f, lq = 0.f;
         for (int j = 0; j < s.ntile; ++j, ++m) {
           const int tt = s.t_begin + j;
@@ -495,18 +520,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc::tc_fence_before();
           tc::mbar_arrive(&bars[kBarSfree + (m & 1)]);
           const int nvalid = s.len - tt * kTile - 64 * w;  // may be <= 0
-          float xv[64];
+          if (nvalid < 64) {  // columns past the sequence end take no weight
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float sv = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
-            xv[c] = (c < nvalid) ? sv * p.scale_log2 : -INFINITY;
+            for (int c = 0; c < 32; ++c) {
+              if (c >= nvalid) sa[c] = __float_as_uint(-INFINITY);
+              if (c + 32 >= nvalid) sb[c] = __float_as_uint(-INFINITY);
+            }
           }
-          float mx[8];  // tree maximum (independent chains)
+          // maximum of the raw scores (the scale is positive, so it commutes with max)
+          float mx[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(xv[i], xv[i + 8]), fmaxf(xv[i + 16], xv[i + 24]));
+          for (int i = 0; i < 16; ++i)
+            mx[i] = fmaxf(tc::max3(__uint_as_float(sa[i]), __uint_as_float(sa[i + 16]), __uint_as_float(sb[i])),
+                          __uint_as_float(sb[i + 16]));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], fmaxf(fmaxf(xv[i + 32], xv[i + 40]), fmaxf(xv[i + 48], xv[i + 56])));
-          float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          for (int i = 0; i < 5; ++i) mx[i] = tc::max3(mx[i], mx[i + 5], mx[i + 10]);
+          float mt = fmaxf(tc::max3(mx[0], mx[1], mx[2]), tc::max3(mx[3], mx[4], mx[15])) * p.scale_log2;
           // tile maximum over both halves (bounded rendezvous of the two warpgroups)
           float* xm = xmax + (m & 1) * 2 * kH;
           xm[w * kH + h] = mt;
@@ -525,19 +554,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             lq *= alpha;
             m_ref = mt;
           }
-          // P = 2^(x - m_ref): bf16 for the value MMA; l sums the fp32 weights,
-          // lq the rounded ones
+          // P = 2^(s scale_log2 - m_ref), one fused multiply-add per pair: bf16 for
+          // the value MMA; l sums the fp32 weights, lq the rounded ones
           uint32_t pk[32];
-          float ls[2] = {0.f, 0.f}, lr[2] = {0.f, 0.f};
+          {
+            const uint64_t c2 = tc::f2(p.scale_log2, p.scale_log2), nm2 = tc::f2(-m_ref, -m_ref);
+            uint64_t la[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)}, qa[2] = {la[0], la[0]};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = tc::ex2(xv[2 * i] - m_ref), p1 = tc::ex2(xv[2 * i + 1] - m_ref);
-            pk[i] = pack_bf16x2(p0, p1);
-            ls[i & 1] += p0 + p1;
-            lr[i & 1] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t u0 = i < 16 ? sa[2 * i] : sb[2 * i - 32], u1 = i < 16 ? sa[2 * i + 1] : sb[2 * i - 31];
+              const float2 x = tc::f2_split(tc::f2_fma(tc::f2u(u0, u1), c2, nm2));
+              const float p0 = tc::ex2(x.x), p1 = tc::ex2(x.y);
+              pk[i] = tc::cvt_bf16x2(p0, p1);
+              la[i & 1] = tc::f2_add(la[i & 1], tc::f2(p0, p1));
+              qa[i & 1] = tc::f2_add(qa[i & 1], tc::f2u(pk[i] << 16, pk[i] & 0xFFFF0000u));
+            }
+            const float2 ls = tc::f2_split(tc::f2_add(la[0], la[1])), lr = tc::f2_split(tc::f2_add(qa[0], qa[1]));
+            l += ls.x + ls.y;
+            lq += lr.x + lr.y;
           }
-          l += ls[0] + ls[1];
-          lq += lr[0] + lr[1];
           if (w < nh) {
             // stage this half's P (+ alpha and per-warp rescale flags); warp 2 + w ships it
             if (sends >= 1 && !tc::wait<false>(&bars[kBarStgFree + w], (sends - 1) & 1, ab)) {
@@ -578,14 +613,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ================================================================ value CTA
     if (warp == 0) {
-      if (lane < 8) {
-        // ---------------------------------------------------------- TMA producer, lane c = column chunk c
-        const int c = lane;
-        if (c == 0) tc::prefetch_map(&cache_map);
+      if (lane == 0) {
+        // ---------------------------------------------------------- TMA producer (one thread)
+        // one 64 KB box per 64-token half tile: its 512 latent columns, chunk-major
+        tc::prefetch_map(&map_v);
         int hh = 0;
         bool ok = true;
         for (int64_t x = lo; x < hi && ok;) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          const Seg s = seg_at(pre, lens, B, x, hi);
           x += s.ntile;
           for (int j = 0; j < s.ntile && ok; ++j) {
             const int tt = s.t_begin + j;
@@ -596,22 +631,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              uint8_t* dst = sm + kOffStage + st * kVStageBytes + c * kChunkBytes;
+              uint8_t* dst = sm + kOffStage + st * kVStageBytes;
               uint64_t* fb = &bars[kBarFull + st];
               if (p.paged) {
                 const int blk = half_block(p, s, tt, w);
                 if (blk < 0) {
                   uint4* z = reinterpret_cast<uint4*>(dst);
-                  for (int i = 0; i < kChunkBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+                  for (int i = 0; i < kVStageBytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
                   tc::fence_async_smem();
                   tc::mbar_arrive(fb);
                   continue;
                 }
-                tc::mbar_expect_tx(fb, kChunkBytes);
-                tc::tma_load_3d(dst, &cache_map, c * 64, 0, blk, fb);
+                tc::mbar_expect_tx(fb, kVStageBytes);
+                tc::tma_load_4d(dst, &map_v, 0, 0, 0, blk, fb);
               } else {
-                tc::mbar_expect_tx(fb, kChunkBytes);
-                tc::tma_load_3d(dst, &cache_map, c * 64, tt * kTile + 64 * w, s.b, fb);
+                tc::mbar_expect_tx(fb, kVStageBytes);
+                tc::tma_load_4d(dst, &map_v, 0, tt * kTile + 64 * w, 0, s.b, fb);
               }
             }
           }
@@ -644,7 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           return tc::wait<false>(&bars[kBarOcomp], (oc++) & 1, ab);
         };
         for (int64_t x = lo; x < hi && ok;) {
-          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          const Seg s = seg_at(pre, lens, B, x, hi);
           x += s.ntile;
           bool first_half = true;
           for (int j = 0; j < s.ntile && ok; ++j) {
@@ -695,7 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int hh = 0;
       bool ok = true;
       for (int64_t x = lo; x < hi && ok;) {
-        const Seg s = seg_at(pre, B, x, hi, p, cap);
+        const Seg s = seg_at(pre, lens, B, x, hi);
         x += s.ntile;
         for (int j = 0; j < s.ntile && ok; ++j) {
           const int tt = s.t_begin + j;
@@ -959,44 +994,36 @@ bool tc_supported(const DecodeLaunch& a) {
 cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap map;
-  cuuint64_t dims[3], strides[2];
-  const cuuint32_t box[3] = {64, 64, 1}, es[3] = {1, 1, 1};
-  dims[0] = kD;
-  strides[0] = (cuuint64_t)kD * 2;
-  if (a.block_table) {
-    dims[1] = 64;
-    dims[2] = (cuuint64_t)a.num_blocks;
-    strides[1] = (cuuint64_t)64 * kD * 2;
-  } else {
-    dims[1] = (cuuint64_t)a.seq_stride;
-    dims[2] = (cuuint64_t)a.batch;
-    strides[1] = (cuuint64_t)a.seq_stride * kD * 2;
-  }
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.pool), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  // The cache as a 4-D tensor (64 columns, tokens, 9 column chunks, sequence or
+  // block): a box spans 64 columns x rows x chunks and lands chunk-major, each
+  // chunk a 128-byte-swizzled K-major tile.
+  const bool paged = a.block_table != nullptr;
+  const cuuint64_t row = (cuuint64_t)kD * 2;
+  const cuuint64_t cdims[4] = {64, paged ? (cuuint64_t)64 : (cuuint64_t)a.seq_stride, 9,
+                               paged ? (cuuint64_t)a.num_blocks : (cuuint64_t)a.batch};
+  const cuuint64_t cstrides[3] = {row, 128, (paged ? (cuuint64_t)64 : (cuuint64_t)a.seq_stride) * row};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  auto encode = [&](CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                    const cuuint64_t* strides, const cuuint32_t* box) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  // score CTA: three chunks of a 128-token tile (contiguous) or one chunk of a 64-token block (paged)
+  CUtensorMap map_s, map_v, q_map, q_map3;
+  const cuuint32_t box_s[4] = {64, paged ? 64u : (cuuint32_t)kTile, paged ? 1u : 3u, 1};
+  // value CTA: the eight latent chunks of 64 tokens
+  const cuuint32_t box_v[4] = {64, 64, 8, 1};
+  // the query [B][128][576]: three chunks of all heads (4-D), or one chunk (3-D)
+  const cuuint64_t qdims[4] = {64, (cuuint64_t)kH, 9, (cuuint64_t)a.batch};
+  const cuuint64_t qstrides[3] = {row, 128, (cuuint64_t)kH * row};
+  const cuuint32_t qbox[4] = {64, 128, 3, 1};
+  const cuuint64_t q3dims[3] = {(cuuint64_t)kD, (cuuint64_t)kH, (cuuint64_t)a.batch};
+  const cuuint64_t q3strides[2] = {row, (cuuint64_t)kH * row};
+  const cuuint32_t q3box[3] = {64, 128, 1};
+  if (!encode(&map_s, a.pool, 4, cdims, cstrides, box_s) || !encode(&map_v, a.pool, 4, cdims, cstrides, box_v) ||
+      !encode(&q_map, a.q, 4, qdims, qstrides, qbox) || !encode(&q_map3, a.q, 3, q3dims, q3strides, q3box))
     return cudaErrorInvalidValue;
-  // the query [B][128][576] for the score CTA's first segment, one box per 64 columns
-  CUtensorMap qmap;
-  {
-    const cuuint64_t qdims[3] = {(cuuint64_t)kD, (cuuint64_t)kH, (cuuint64_t)a.batch};
-    const cuuint64_t qstrides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kH * kD * 2};
-    const cuuint32_t qbox[3] = {64, 128, 1};
-    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qdims, qstrides, qbox, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  // the score CTA's whole-tile boxes (contiguous cache only)
-  CUtensorMap map128 = map;
-  if (!a.block_table) {
-    const cuuint32_t box128[3] = {64, 128, 1};
-    if (enc(&map128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.pool), dims, strides, box128, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
   TcParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.pool = static_cast<const __nv_bfloat16*>(a.pool);
@@ -1018,7 +1045,7 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(a.batch);
   cudaError_t e = ensure_smem<decode_tc_kernel>((int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map, map128, qmap, p);
+  decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map_s, map_v, q_map, q_map3, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 grid(kDC / 16, a.batch);

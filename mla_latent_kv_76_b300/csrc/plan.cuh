@@ -207,6 +207,70 @@ MLA_DEVI bool plan_prefix(const int* pre, int B, int G, int* W) {
   return prefer_aligned(cost_aligned, T, G, s_tmin);
 }
 
+// One warp builds the whole plan (tensor-core decode prologue): validated
+// lengths lens[0..B), tile prefix pre[0..B] and entry prefix W[0..B] in shared
+// memory, the same values as tile_prefix + plan_prefix; every lane returns
+// whether the sequence-aligned plan is preferred.  Only warp shuffles and
+// __syncwarp: no block-wide barrier, so the other warps of the block can set up
+// barriers and tensor memory meanwhile (the block-wide version cost ~2 us of
+// serial barriers and loops at the start of every CTA).
+MLA_DEVI bool warp_plan(const int32_t* seqlens, int B, int64_t cap, int32_t* status, int G, int tile, int* lens,
+                        int* pre, int* W) {
+  const int lane = threadIdx.x & 31;
+  for (int b = lane; b < B; b += 32) lens[b] = effective_len(seqlens, b, cap, status);
+  __syncwarp();
+  const int per = (B + 31) / 32, b0 = min(B, lane * per), b1 = min(B, b0 + per);
+  int tl = 0, n = 0, tmin = INT_MAX;
+  for (int b = b0; b < b1; ++b) {
+    const int t = tiles_of(lens[b], tile);
+    tl += t;
+    if (t > 0) {
+      ++n;
+      tmin = min(tmin, t);
+    }
+  }
+  int incl = tl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    n += __shfl_xor_sync(0xffffffffu, n, o);
+    tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+  }
+  const int T = __shfl_sync(0xffffffffu, incl, 31);
+  int run = incl - tl, wl = 0, cost = 0;
+  for (int b = b0; b < b1; ++b) {
+    pre[b] = run;
+    const int t = tiles_of(lens[b], tile);
+    run += t;
+    const int w = plan_entries(t, T, n, G);
+    wl += w;
+    if (w > 0) cost = max(cost, (t + w - 1) / w);
+  }
+  int winc = wl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, winc, o);
+    if (lane >= o) winc += v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cost = max(cost, __shfl_xor_sync(0xffffffffu, cost, o));
+  int wr = winc - wl;
+  for (int b = b0; b < b1; ++b) {
+    W[b] = wr;
+    wr += plan_entries(tiles_of(lens[b], tile), T, n, G);
+  }
+  if (lane == 31) {
+    pre[B] = T;
+    W[B] = winc;
+  }
+  __syncwarp();
+  return prefer_aligned(cost, T, G, tmin);
+}
+
 // The sequence owning entry e < W[B]: the largest b with W[b] <= e.
 MLA_HD int seq_of_entry(const int* W, int B, int64_t e) { return seq_of_tile(W, B, e); }
 
