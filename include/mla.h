@@ -158,7 +158,10 @@ enum {
  *   lse_out  [batch][n_h] fp32, natural log; may be NULL
  * Sequence lengths above the cache capacity, or block ids outside
  * [0, num_blocks), are treated as empty / zero rows and reported through
- * dev_status.  Requires n_h <= 128, d_c in {64, 128, 256, 512},
+ * dev_status.  If a bounded device-side wait gives up (MLA_ERR_DEVICE_TIMEOUT
+ * in dev_status), the tensor-core path writes NaN to z_out and lse_out; the
+ * outputs of a call whose dev_status is non-zero are otherwise not defined
+ * beyond the rules above.  Requires n_h <= 128, d_c in {64, 128, 256, 512},
  * (d_c + d_R) a multiple of 16, block_tokens == 64 for a paged cache.
  */
 int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const void* pool,
@@ -179,15 +182,18 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
  * partials in a file-scope device array of MLA_NOALLOC_SCRATCH_BYTES (64 MiB)
  * that every GPU which loads the library holds until the process exits.
  *  - Arguments are those of mla_decode_attn without workspace/workspace_bytes.
- *  - If mla_decode_workspace_size(dims, batch, num_workers) is larger than
+ *  - If the workspace this call needs (mla_decode_workspace_size for the
+ *    worker count the call uses: num_workers, else the automatic count of
+ *    its path, one per SM pair on the tensor-core path) is larger than
  *    MLA_NOALLOC_SCRATCH_BYTES the call returns MLA_ERR_WORKSPACE and
  *    enqueues nothing.  (On a 148-SM B300 with 128 heads, d_c = 512 and
- *    automatic workers this allows up to 107 sequences; passing an explicit,
+ *    automatic workers this allows up to 180 sequences; passing an explicit,
  *    smaller num_workers allows more.)
  *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *    on the current device, so a context re-created after a device reset
+ *    gets its own array.  The first lookup on a device loads the library's
+ *    device code there; make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents.
  *    Nothing in it has to start at zero: each call writes every partial it
  *    reads back.  Calls whose GPU work overlaps (other streams, or threads

@@ -46,15 +46,17 @@ bool dims_basic_ok(const mla_dims* d) {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t off_o, off_lse, off_l, off_lq, total;
+  size_t off_plan, off_o, off_lse, off_l, off_lq, total;
 };
 
-// Workspace: a 256-byte header, then per split-KV partial slot (worker g +
-// sequence b) the latent vector o [n_h][d_c] and three per-head scalars.
+// Workspace: a header (64 bytes of plan scalars, then two int32 per sequence:
+// the partial slots the combine reads), then per split-KV partial slot (worker
+// g + sequence b) the latent vector o [n_h][d_c] and three per-head scalars.
 WsLayout ws_layout(const mla_dims& d, int batch, int workers) {
   WsLayout w;
   const size_t slots = (size_t)workers + (size_t)batch;
-  w.off_o = 256;
+  w.off_plan = 64;
+  w.off_o = align256(w.off_plan + 8 * (size_t)batch);
   w.off_lse = w.off_o + align256(slots * d.n_heads * d.d_latent * sizeof(float));
   w.off_l = w.off_lse + align256(slots * d.n_heads * sizeof(float));
   w.off_lq = w.off_l + align256(slots * d.n_heads * sizeof(float));
@@ -130,6 +132,37 @@ int mla_append_cache(const mla_dims* dims, int32_t n_tokens, int32_t d_model, co
                                       pool, dev_status, as_stream(stream)));
 }
 
+}  // extern "C"
+
+namespace mla {
+
+// The split-KV worker count a decode call uses: the caller's, else one per SM
+// pair on the tensor-core path and auto_workers on the shape-generic path.
+int decode_workers(const mla_dims& d, int batch, int num_workers, int flags, int sms) {
+  if (num_workers > 0) return num_workers;
+  DecodeLaunch a;
+  a.n_heads = d.n_heads;
+  a.d_latent = d.d_latent;
+  a.d_rope = d.d_rope;
+  a.batch = batch;
+  const bool use_tc = !(flags & MLA_DECODE_FORCE_GENERIC) && tc_supported(a);
+  return use_tc ? (sms / 2 > 0 ? sms / 2 : 1) : auto_workers(d, sms);
+}
+
+size_t decode_workspace_bytes(const mla_dims* dims, int batch, int num_workers, int flags) {
+  int why = 0;
+  if (!decode_dims_ok(dims, &why) || batch < 0 || batch > kMaxBatch || num_workers < 0 ||
+      num_workers > kMaxWorkers || (flags & ~MLA_DECODE_FORCE_GENERIC))
+    return 0;
+  const int sms = num_workers > 0 ? 1 : device_sm_count();
+  if (sms <= 0) return 0;
+  return ws_layout(*dims, batch, decode_workers(*dims, batch, num_workers, flags, sms)).total;
+}
+
+}  // namespace mla
+
+extern "C" {
+
 size_t mla_decode_workspace_size(const mla_dims* dims, int32_t batch, int32_t num_workers) {
   int why = 0;
   if (!decode_dims_ok(dims, &why) || batch < 0 || batch > mla::kMaxBatch || num_workers < 0 ||
@@ -173,7 +206,7 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.d_rope = dims->d_rope;
   a.batch = batch;
   const bool use_tc = !(flags & MLA_DECODE_FORCE_GENERIC) && mla::tc_supported(a);
-  const int G = num_workers > 0 ? num_workers : (use_tc ? (sms / 2 > 0 ? sms / 2 : 1) : auto_workers(*dims, sms));
+  const int G = mla::decode_workers(*dims, batch, num_workers, flags, sms);
   const WsLayout w = ws_layout(*dims, batch, G);
   if (!workspace || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
@@ -188,7 +221,8 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.scale = scale;
   a.workers = G;
   a.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_o);
-  a.plan_flag = static_cast<int32_t*>(workspace);  // first word of the 256-byte header
+  a.plan_flag = static_cast<int32_t*>(workspace);  // header words: plan kind, tiles, workers
+  a.seqplan = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + w.off_plan);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lse);
   a.l_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_l);
   a.lq_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.off_lq);

@@ -1,8 +1,6 @@
 // mla_decode_attn_noalloc: decode for callers that cannot allocate device
 // memory.  It runs the regular decode entry point with its workspace placed in
 // a file-scope device array, so the caller passes only inputs and outputs.
-#include <mutex>
-
 #include "../../include/mla.h"
 #include "kernels.h"
 
@@ -12,23 +10,14 @@ namespace {
 // this array until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDev = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDev] = {};
-
-// Device address of the array on the current device, looked up once per
-// device (with that device current).  Host code must not use the array's name
+// Device address of the array on the current device, looked up on every call
+// (cheap), so that a context re-created after a device reset gets its own
+// array rather than a stale address.  Host code must not use the array's name
 // as an address: on the host it is only a stand-in symbol.
 int scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MLA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
+  *out = p;
   return MLA_OK;
 }
 
@@ -41,7 +30,8 @@ extern "C" int mla_decode_attn_noalloc(const mla_dims* dims, int32_t batch, cons
                                        int32_t z_is_fp32, float* lse_out, int32_t* dev_status, void* stream) {
   if (!dims || batch < 0) return MLA_ERR_INVALID_ARG;
   if (batch == 0) return MLA_OK;
-  const size_t need = mla_decode_workspace_size(dims, batch, num_workers);
+  // sized for the worker count this call will use
+  const size_t need = mla::decode_workspace_bytes(dims, batch, num_workers, flags);
   if (need == 0) {
     // invalid or unsupported arguments: let the regular entry point name the error
     return mla_decode_attn(dims, batch, q, pool, block_table, max_blocks_per_seq, num_blocks,

@@ -125,7 +125,8 @@ struct TcParams {
   float* l_part;    // [(G + B)][128]       sum of the fp32 weights relative to m_part (for lse)
   float* lq_part;   // [(G + B)][128]       sum of the bf16-rounded weights the MMA used (normalises z)
   int32_t* status;
-  int32_t* plan_flag;  // 1: sequence-aligned plan, 0: even tile split (read by the combine)
+  int32_t* plan_hdr;   // [plan kind (1: sequence-aligned, 0: even tile split), tiles T, workers G] for the combine
+  int32_t* seqplan;    // [B][2] for the combine: sequence b's partial slots (aligned) or workers (even split)
 };
 
 struct Seg {
@@ -193,8 +194,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       range[0] = al ? entry_tile(pre, Wp, B, div_floor((int64_t)g * E, G)) : worker_begin(g, T, G);
       range[1] = al ? entry_tile(pre, Wp, B, div_floor((int64_t)(g + 1) * E, G)) : worker_begin(g + 1, T, G);
       *aligned_s = al ? 1 : 0;
-      if (blockIdx.x == 0) *p.plan_flag = al ? 1 : 0;
+      if (blockIdx.x == 0) {
+        p.plan_hdr[0] = al ? 1 : 0;
+        p.plan_hdr[1] = (int)T;
+        p.plan_hdr[2] = G;
+      }
     }
+    if (blockIdx.x == 0) {
+      // which partials the combine merges for each sequence: slots first..last of
+      // the aligned plan, or the workers first..last of the even split (slot g + b;
+      // workers without tiles in between wrote nothing); last < first: no tiles
+      const int B = p.batch, G = p.workers, T = pre[B];
+      for (int b = lane; b < B; b += 32) {
+        const int t = pre[b + 1] - pre[b];
+        int first = 0, last = -1;
+        if (t > 0) {
+          first = al ? Wp[b] : worker_of(pre[b], T, G);
+          last = al ? Wp[b + 1] - 1 : worker_of(pre[b + 1] - 1, T, G);
+        }
+        p.seqplan[2 * b] = first;
+        p.seqplan[2 * b + 1] = last;
+      }
+    }
+    // the combine may be scheduled now; it waits for this grid to finish before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   } else if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 512);
   } else if (tid == 64) {
@@ -829,75 +852,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // 512 contiguous bytes per warp.
 template <bool ZF32>
 __global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
-  const int jg = blockIdx.x, b = blockIdx.y, h = threadIdx.x, warp = h >> 5, lane = h & 31;
-  const int G = a.workers;
+  const int jg = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
+  // launched as a programmatic dependent of the partial pass: wait for it (and
+  // its memory) before reading anything it wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* m_part = a.lse_part;
   const float* l_part = a.l_part;
   const float* lq_part = a.lq_part;
-  const int64_t cap = a.block_table ? (int64_t)a.max_blocks * 64 : a.seq_stride;
-  // the split plan of the partial kernel: total tiles T, non-empty sequences n,
-  // then the entries of the sequences before b (W_b) and of b itself
-  __shared__ long long red[2][4];
-  __shared__ long long s_tot[2];
-  long long total = 0, nonempty = 0;
-  for (int i = h; i < a.batch; i += blockDim.x) {
-    const int t = tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile);
-    total += t;
-    nonempty += t > 0;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    total += __shfl_xor_sync(0xffffffffu, total, o);
-    nonempty += __shfl_xor_sync(0xffffffffu, nonempty, o);
-  }
-  if (lane == 0) {
-    red[0][warp] = total;
-    red[1][warp] = nonempty;
-  }
-  __syncthreads();
-  if (h == 0) {
-    s_tot[0] = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-    s_tot[1] = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  }
-  __syncthreads();
-  const int64_t T = s_tot[0];
-  const int n_ne = (int)s_tot[1];
-  long long before = 0, tiles_before = 0;
-  for (int i = h; i < b; i += blockDim.x) {
-    const int t = tiles_of(effective_len(a.seqlens, i, cap, nullptr), kTile);
-    before += plan_entries(t, T, n_ne, G);
-    tiles_before += t;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    tiles_before += __shfl_xor_sync(0xffffffffu, tiles_before, o);
-  }
-  __syncthreads();  // red[] is reused
-  if (lane == 0) {
-    red[0][warp] = before;
-    red[1][warp] = tiles_before;
-  }
-  __syncthreads();
-  const int64_t Wb = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-  const int64_t Sb = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  const bool aligned = *a.plan_flag != 0;
-  const int nb = tiles_of(effective_len(a.seqlens, b, cap, nullptr), kTile);
+  // the partial pass's plan: kind, tiles, workers, and this sequence's partials
+  const bool aligned = a.plan_flag[0] != 0;
+  const int T = a.plan_flag[1], G = a.plan_flag[2];
+  const int64_t g0 = a.seqplan[2 * b], g1 = a.seqplan[2 * b + 1];
   // this block: latent columns [16 jg, 16 jg + 16) of every head of sequence b
   float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 16;
   __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC + jg * 16;
-  if (nb == 0) {
+  // a partial pass that gave up on a bounded wait left partials unwritten: the
+  // outputs are NaN then, not stale numbers
+  const bool failed = a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) == MLA_ERR_DEVICE_TIMEOUT;
+  if (g1 < g0 || failed) {
+    const float zv = failed ? __int_as_float(0x7fc00000) : 0.f;
     for (int d = 0; d < 16; ++d) {
-      if (ZF32) zf[d] = 0.f; else zb[d] = __float2bfloat16_rn(0.f);
+      if (ZF32) zf[d] = zv; else zb[d] = __float2bfloat16_rn(zv);
     }
-    if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = -INFINITY;
+    if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = failed ? zv : -INFINITY;
     return;
   }
-  // sequence b's partials: slots [Wb, Wb + wb) (aligned plan, every one written),
-  // or slot g + b of each worker g whose tiles touch b (even split; a worker with
-  // no tiles wrote nothing)
-  const int64_t g0 = aligned ? Wb : worker_of(Sb, T, G);
-  const int64_t g1 = aligned ? Wb + plan_entries(nb, T, n_ne, G) - 1 : worker_of(Sb + nb - 1, T, G);
   // partials four at a time, all their loads in flight together; the running
   // maximum M moves as chunks arrive (acc and L rescaled by 2^(M_old - M_new))
   float M = -INFINITY, L = 0.f, Lq = 0.f;
@@ -1041,17 +1020,27 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   p.l_part = a.l_part;
   p.lq_part = a.lq_part;
   p.status = a.status;
-  p.plan_flag = a.plan_flag;
+  p.plan_hdr = a.plan_flag;
+  p.seqplan = a.seqplan;
   const size_t smem = tc_smem_bytes(a.batch);
   cudaError_t e = ensure_smem<decode_tc_kernel>((int)smem);
   if (e != cudaSuccess) return e;
   decode_tc_kernel<<<2 * a.workers, kThreads, smem, s>>>(map_s, map_v, q_map, q_map3, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid(kDC / 16, a.batch);
-  if (a.z_is_fp32) combine_tc_kernel<true><<<grid, 128, 0, s>>>(a);
-  else combine_tc_kernel<false><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  // the combine as a programmatic dependent launch: its blocks are scheduled as
+  // the partial pass's CTAs exit instead of after the whole grid has drained
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kDC / 16, a.batch);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.z_is_fp32 ? cudaLaunchKernelEx(&cfg, combine_tc_kernel<true>, a)
+                     : cudaLaunchKernelEx(&cfg, combine_tc_kernel<false>, a);
 }
 
 }  // namespace mla

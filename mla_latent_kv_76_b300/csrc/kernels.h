@@ -56,7 +56,8 @@ struct DecodeLaunch {
   float* lse_part;        // [(G + B)][n_h]  generic: lse; tensor-core: reference maximum (log2)
   float* l_part;          // [(G + B)][n_h]  tensor-core: fp32 weight sum relative to the maximum
   float* lq_part;         // [(G + B)][n_h]  tensor-core: bf16-rounded weight sum relative to the maximum
-  int32_t* plan_flag;     // tensor-core: which split plan the partial pass used (workspace header)
+  int32_t* plan_flag;     // tensor-core: workspace header words [plan kind (1 = sequence-aligned), tiles, workers]
+  int32_t* seqplan;       // tensor-core: [B][2] partials of sequence b: slots (aligned) or workers (even split) first..last
   void* z_out;
   int32_t z_is_fp32;
   float* lse_out;
@@ -71,6 +72,12 @@ int generic_head_groups(int n_heads);
 // Tensor-core (tcgen05) decode for n_h = 128, d_c = 512, d_R = 64, partial pass
 // and its combine: `workers` is the number of CTA pairs (clusters of two).
 bool tc_supported(const DecodeLaunch& a);
+
+// Split-KV workers a decode call uses (num_workers, else the automatic count
+// for its path on a device with `sms` SMs), and the workspace bytes it needs
+// (0 for arguments mla_decode_attn rejects).
+int decode_workers(const mla_dims& d, int batch, int num_workers, int flags, int sms);
+size_t decode_workspace_bytes(const mla_dims* dims, int batch, int num_workers, int flags);
 cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s);
 size_t generic_smem_bytes(int D, int batch);
 

@@ -85,3 +85,22 @@ def test_noalloc_rejects_requests_beyond_its_scratch(mla):
     assert e.value.code == mla.MLA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert bool((z == 7.0).all())             # nothing was enqueued
+
+
+def test_noalloc_sizes_its_check_by_the_workers_it_uses(mla):
+    # 150 sequences: above the limit for one worker per SM (the conservative
+    # mla_decode_workspace_size(..., 0)), inside it for the tensor-core path's
+    # one worker per SM pair, which is what the call launches
+    B = 150
+    wl = mi.make_random(35, 128, 512, 64, [1 + (7 * b) % 300 for b in range(B)], paged=False)
+    dims = mla.Dims.of(wl)
+    assert mla.mla_decode_workspace_size(dims, B, 0) > mla.MLA_NOALLOC_SCRATCH_BYTES
+    a = _inputs(wl)
+    z_ref, lse_ref = mla.mla_decode_attn(dims, a["q"], a["pool"], a["seqlens"], wl.scale, seq_stride=wl.seq_stride)
+    z = torch.empty_like(z_ref)
+    lse = torch.empty_like(lse_ref)
+    mla.mla_decode_attn_noalloc(dims, a["q"], a["pool"], a["seqlens"], wl.scale, seq_stride=wl.seq_stride,
+                                z_out=z, lse_out=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(z.view(torch.int32), z_ref.view(torch.int32)), "z noalloc vs regular"
+    assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32)), "lse noalloc vs regular"
