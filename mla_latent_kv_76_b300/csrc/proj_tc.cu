@@ -241,14 +241,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // ---------------------------------------------------------------- cache append
-// [c; k^R] = [W^DKV; W^KR] h for up to 32 new tokens ("MLA 的核心结构": c^KV =
-// W^DKV h; "RoPE 为什么要解耦": k^R = RoPE(W^KR h)), tokens as M (padded to 128).
+// [c; k^R] = [W^DKV; W^KR] h for the new tokens ("MLA 的核心结构": c^KV =
+// W^DKV h; "RoPE 为什么要解耦": k^R = RoPE(W^KR h)), tokens as M.
 // A cluster of kAppendSplit CTAs shares one 96-column slice of the 576 outputs,
 // each CTA one 448-deep slice of d_model (7 boxes of 64): 6 x 16 = 96 CTAs
-// stream the 8.3 MB weight once, all of it in flight at the same time.  The
-// fp32 partial tiles are summed in rank order through distributed shared
-// memory, each rank finishing 6 of the 96 columns: RoPE on the k^R pairs,
-// bf16 rounding, and the write into the cache slot of (sequence, position).
+// stream the 8.3 MB weight once, all of it in flight at the same time, and
+// keep their weight slice in shared memory for every token tile.  Tokens come
+// in tiles of `rows` (up to 32 tokens: one tile of the count rounded up to 8;
+// more: tiles of 128, the last one padded with zero rows by the TMA fill).
+// Per tile, the fp32 partials are summed in rank order through distributed
+// shared memory, each rank finishing 6 of the 96 columns: RoPE on the k^R
+// pairs, bf16 rounding, and the write into the cache slot of (sequence,
+// position).
 constexpr int kAppendSplit = 16;
 MLA_DEVI float ld_cluster_f32(uint32_t a) {
   float x;
@@ -257,6 +261,7 @@ MLA_DEVI float ld_cluster_f32(uint32_t a) {
 }
 constexpr int kAppendN = 96;
 constexpr int kAppendKBoxes = 7;
+constexpr int kAppendBigRows = 128;
 
 struct AppendParams {
   int n_tokens, d_model;
@@ -273,24 +278,28 @@ struct AppendParams {
 
 __global__ void __launch_bounds__(kThreads, 1)
     append_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
-                     const __grid_constant__ AppendParams p, int rows8) {
+                     const __grid_constant__ AppendParams p, int rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bars[2];
+  __shared__ uint64_t bars[3];  // weight slice, token tile, MMAs done
   __shared__ uint32_t tmem_slot;
-  __shared__ float red[kAppendN * 32];  // this CTA's partial tile, [column][token t < 32]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = tc::cluster_rank();
   const int ntile = (int)(blockIdx.x / kAppendSplit);
   const int n0 = ntile * kAppendN;
   const int k0 = (int)rank * kAppendKBoxes * 64;
-  const int hbytes = rows8 * 128;
+  const int hbytes = rows * 128;
   const int wbytes = kAppendN * 128;
-  uint8_t* sh = sm;                                                    // [7][rows8 x 128 B]
+  const int mtiles = (p.n_tokens + rows - 1) / rows;
+  uint8_t* sh = sm;                                                    // [7][rows x 128 B]
   uint8_t* sw = sm + ((kAppendKBoxes * hbytes + 1023) & ~1023);        // [7][96 x 128 B]
+  // once a tile's MMAs are done its token boxes hold this CTA's fp32 partial
+  // tile, [column][token] (96 x rows floats fit in 7 x rows x 128 bytes)
+  float* red = reinterpret_cast<float*>(sh);
   if (tid == 0) {
-    tc::mbar_init(&bars[0], 2 * kAppendKBoxes);  // one arrival per issuing lane
-    tc::mbar_init(&bars[1], 1);
+    tc::mbar_init(&bars[0], kAppendKBoxes);  // one arrival per issuing thread
+    tc::mbar_init(&bars[1], kAppendKBoxes);
+    tc::mbar_init(&bars[2], 1);
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
@@ -301,87 +310,94 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < kAppendKBoxes) {
     tc::mbar_expect_tx(&bars[0], wbytes);
     tc::tma_load_2d(sw + tid * wbytes, &map_w, k0 + 64 * tid, n0, &bars[0]);
-  } else if (tid < 2 * kAppendKBoxes) {
-    const int j = tid - kAppendKBoxes;
-    tc::mbar_expect_tx(&bars[0], hbytes);
-    tc::tma_load_2d(sh + j * hbytes, &map_h, k0 + 64 * j, 0, &bars[0]);
   }
-  if (tid == 0) {
-    bool ok = wait_done(&bars[0], 0);
-    if (ok) {
-      tc::tc_fence_after();
-      constexpr uint32_t id = tc::idesc_bf16(128, kAppendN, 0, 0);
-      const uint32_t ha = smem_u32(sh), wa = smem_u32(sw);
-#pragma unroll
-      for (int ks = 0; ks < 4 * kAppendKBoxes; ++ks)
-        tc::mma_ss(tb, tc::smem_desc(ha + (ks >> 2) * hbytes + (ks & 3) * 32, 16, 1024),
-                   tc::smem_desc(wa + (ks >> 2) * wbytes + (ks & 3) * 32, 16, 1024), id, ks > 0 ? 1u : 0u);
-      tc::mma_commit(&bars[1]);
-      ok = wait_done(&bars[1], 0);
-    }
-    if (!ok) report(p.status, MLA_ERR_DEVICE_TIMEOUT);
-  }
-  __syncthreads();
-  tc::tc_fence_after();
-  __syncwarp();
-  if (warp == 0) {  // token rows t < 32 live in TMEM lanes 0..31
-    uint32_t r[32];
-#pragma unroll
-    for (int c = 0; c < kAppendN / 32; ++c) {
-      tc::tmem_ld32(tb + c * 32, r);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) red[(c * 32 + i) * 32 + lane] = __uint_as_float(r[i]);
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::cluster_sync();
-  // rank r finishes columns [n0 + 6 r, n0 + 6 r + 6) of every token: sum the 16
-  // partials in rank order, RoPE the k^R pairs, round, scatter into the cache
   constexpr int kCols = kAppendN / kAppendSplit;
-  for (int idx = tid; idx < p.n_tokens * (kCols / 2); idx += kThreads) {
-    const int t = idx / (kCols / 2), cp = idx % (kCols / 2);
-    const int cl = (int)rank * kCols + 2 * cp;  // local column (even)
-    float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-    for (int q = 0; q < kAppendSplit; ++q) {
-      v0 += ld_cluster_f32(tc::map_peer(&red[cl * 32 + t], (uint32_t)q));
-      v1 += ld_cluster_f32(tc::map_peer(&red[(cl + 1) * 32 + t], (uint32_t)q));
+  for (int mt = 0; mt < mtiles; ++mt) {
+    if (tid < kAppendKBoxes) {
+      tc::mbar_expect_tx(&bars[1], hbytes);
+      tc::tma_load_2d(sh + tid * hbytes, &map_h, k0 + 64 * tid, mt * rows, &bars[1]);
     }
-    const int n = n0 + cl;
-    const int s = p.seq_idx[t], ps = p.pos[t];
-    bool ok = (s >= 0) && (s < p.n_seqs) && (ps >= 0);
-    int64_t row = 0;
-    if (ok) {
-      if (p.block_table) {
-        const int lb = ps / p.block_tokens;
-        ok = lb < p.max_blocks;
-        if (ok) {
-          const int blk = p.block_table[(int64_t)s * p.max_blocks + lb];
-          ok = (blk >= 0) && (blk < p.num_blocks);
-          row = (int64_t)blk * p.block_tokens + ps % p.block_tokens;
-        }
-      } else {
-        ok = ps < p.seq_stride;
-        row = (int64_t)s * p.seq_stride + ps;
+    if (tid == 0) {
+      bool ok = (mt > 0 || wait_done(&bars[0], 0)) && wait_done(&bars[1], mt & 1);
+      if (ok) {
+        tc::tc_fence_after();
+        constexpr uint32_t id = tc::idesc_bf16(128, kAppendN, 0, 0);
+        const uint32_t ha = smem_u32(sh), wa = smem_u32(sw);
+        // M = 128 token rows; with rows < 128 the rows past the tile read other
+        // operands' bytes and their results are not used
+#pragma unroll
+        for (int ks = 0; ks < 4 * kAppendKBoxes; ++ks)
+          tc::mma_ss(tb, tc::smem_desc(ha + (ks >> 2) * hbytes + (ks & 3) * 32, 16, 1024),
+                     tc::smem_desc(wa + (ks >> 2) * wbytes + (ks & 3) * 32, 16, 1024), id, ks > 0 ? 1u : 0u);
+        tc::mma_commit(&bars[2]);
+        ok = wait_done(&bars[2], mt & 1);
+      }
+      if (!ok) report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    if (32 * warp < rows) {  // token rows 32 w .. 32 w + 31 live in TMEM lanes of warp w
+      const int t = 32 * warp + lane;
+      uint32_t r[32];
+#pragma unroll
+      for (int c = 0; c < kAppendN / 32; ++c) {
+        tc::tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + c * 32, r);
+        tc::tmem_wait_ld();
+        if (t < rows)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red[(c * 32 + i) * rows + t] = __uint_as_float(r[i]);
       }
     }
-    if (!ok) {
-      report(p.status, MLA_ERR_DEVICE_BOUNDS);
-      continue;
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::cluster_sync();
+    // rank r finishes columns [n0 + 6 r, n0 + 6 r + 6) of the tile's tokens: sum
+    // the 16 partials in rank order, RoPE the k^R pairs, round, scatter into the cache
+    const int nt = min(rows, p.n_tokens - mt * rows);
+    for (int idx = tid; idx < nt * (kCols / 2); idx += kThreads) {
+      const int t = idx / (kCols / 2), cp = idx % (kCols / 2);
+      const int cl = (int)rank * kCols + 2 * cp;  // local column (even)
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < kAppendSplit; ++q) {
+        v0 += ld_cluster_f32(tc::map_peer(&red[cl * rows + t], (uint32_t)q));
+        v1 += ld_cluster_f32(tc::map_peer(&red[(cl + 1) * rows + t], (uint32_t)q));
+      }
+      const int n = n0 + cl;
+      const int tok = mt * rows + t;
+      const int s = p.seq_idx[tok], ps = p.pos[tok];
+      bool ok = (s >= 0) && (s < p.n_seqs) && (ps >= 0);
+      int64_t row = 0;
+      if (ok) {
+        if (p.block_table) {
+          const int lb = ps / p.block_tokens;
+          ok = lb < p.max_blocks;
+          if (ok) {
+            const int blk = p.block_table[(int64_t)s * p.max_blocks + lb];
+            ok = (blk >= 0) && (blk < p.num_blocks);
+            row = (int64_t)blk * p.block_tokens + ps % p.block_tokens;
+          }
+        } else {
+          ok = ps < p.seq_stride;
+          row = (int64_t)s * p.seq_stride + ps;
+        }
+      }
+      if (!ok) {
+        report(p.status, MLA_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      if (n >= 512) {
+        float c, sn;
+        const int i = (n - 512) >> 1;
+        rope_cos_sin(ps, p.rope.hi[i], p.rope.lo[i], &c, &sn);
+        const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
+        v0 = r0;
+        v1 = r1;
+      }
+      *reinterpret_cast<uint32_t*>(p.pool + row * 576 + n) = pack_bf16x2(v0, v1);
     }
-    if (n >= 512) {
-      float c, sn;
-      const int i = (n - 512) >> 1;
-      rope_cos_sin(ps, p.rope.hi[i], p.rope.lo[i], &c, &sn);
-      const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
-      v0 = r0;
-      v1 = r1;
-    }
-    *reinterpret_cast<uint32_t*>(p.pool + row * 576 + n) = pack_bf16x2(v0, v1);
+    tc::cluster_sync();  // peers keep their partials until every rank has read them
   }
-  tc::cluster_sync();  // peers keep their partials until every rank has read them
   if (warp == 0) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tb, 128);
@@ -433,25 +449,29 @@ bool make_map2(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
 
 }  // namespace
 
-int append_smem_bytes(int rows8) {
-  return ((kAppendKBoxes * rows8 * 128 + 1023) & ~1023) + kAppendKBoxes * kAppendN * 128 + 1024;
+int append_smem_bytes(int rows) {
+  return ((kAppendKBoxes * rows * 128 + 1023) & ~1023) + kAppendKBoxes * kAppendN * 128 + 1024;
 }
+int append_rows(int n_tokens) { return n_tokens <= 32 ? (n_tokens + 7) & ~7 : kAppendBigRows; }
 
-// True when a cluster of 16 CTAs of the append kernel can be resident on this
-// device (a non-portable cluster size: it needs 16 free SMs in one GPC).
-// Decided once per device; also sets the kernel's attributes there.
-bool append_cluster_fits() {
-  static int fits_dev[64];  // 0 unknown, 1 no, 2 yes
+// True when a cluster of 16 CTAs of the append kernel with the shared memory
+// of `rows`-token tiles can be resident on this device (a non-portable
+// cluster size: it needs 16 free SMs in one GPC).  Decided once per device
+// for each of the two tile sizes; also sets the kernel's attributes there.
+bool append_cluster_fits(int rows) {
+  static int fits_dev[64][2];  // 0 unknown, 1 no, 2 yes; [small tiles, 128-token tiles]
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lk(mu);
-  int& fits = fits_dev[dev];
+  const bool big = rows > 32;
+  int& fits = fits_dev[dev][big ? 1 : 0];
   if (fits) return fits == 2;
   fits = 1;
-  const int smem = append_smem_bytes(32);
+  const int smem = append_smem_bytes(big ? kAppendBigRows : 32);
   if (cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
-      cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           append_smem_bytes(kAppendBigRows)) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
@@ -476,18 +496,18 @@ bool append_cluster_fits() {
 }
 
 bool append_tc_supported(const mla_dims& d, int n_tokens, int d_model) {
-  return d.d_latent == 512 && d.d_rope == 64 && n_tokens >= 1 && n_tokens <= 32 &&
-         d_model == kAppendSplit * kAppendKBoxes * 64 && append_cluster_fits();
+  return d.d_latent == 512 && d.d_rope == 64 && n_tokens >= 1 && d_model == kAppendSplit * kAppendKBoxes * 64 &&
+         append_cluster_fits(append_rows(n_tokens));
 }
 
 cudaError_t launch_append_tc(const mla_dims& d, int n_tokens, int d_model, const void* h, const void* w,
                              const int32_t* seq_idx, const int32_t* pos, int n_seqs, const int32_t* block_table,
                              int max_blocks, int num_blocks, int64_t seq_stride, void* pool, int32_t* status,
                              cudaStream_t s) {
-  const int rows8 = (n_tokens + 7) & ~7;
+  const int rows = append_rows(n_tokens);
   CUtensorMap mw, mh;
   if (!make_map2(&mw, w, (uint64_t)d_model, 576, (uint64_t)d_model * 2, kAppendN) ||
-      !make_map2(&mh, h, (uint64_t)d_model, (uint64_t)n_tokens, (uint64_t)d_model * 2, rows8))
+      !make_map2(&mh, h, (uint64_t)d_model, (uint64_t)n_tokens, (uint64_t)d_model * 2, rows))
     return cudaErrorInvalidValue;
   AppendParams p;
   p.n_tokens = n_tokens;
@@ -503,7 +523,7 @@ cudaError_t launch_append_tc(const mla_dims& d, int n_tokens, int d_model, const
   p.pool = static_cast<__nv_bfloat16*>(pool);
   rope_turns_host(d.rope_base, 64, &p.rope);
   p.status = status;
-  const int smem = append_smem_bytes(rows8);
+  const int smem = append_smem_bytes(rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((576 / kAppendN) * kAppendSplit);
   cfg.blockDim = dim3(kThreads);
@@ -516,7 +536,7 @@ cudaError_t launch_append_tc(const mla_dims& d, int n_tokens, int d_model, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, append_tc_kernel, mw, mh, p, rows8);
+  return cudaLaunchKernelEx(&cfg, append_tc_kernel, mw, mh, p, rows);
 }
 
 bool proj_tc_supported(const mla_dims& d, int batch, bool absorb) {

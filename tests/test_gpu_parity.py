@@ -278,11 +278,13 @@ def test_append_values_and_bounds(mla):
     assert np.array_equal(dev_to_bits(pool), before)
 
 
-@pytest.mark.parametrize("n_tok,paged", [(1, True), (7, False), (16, True), (31, False), (32, True), (33, False)])
+@pytest.mark.parametrize("n_tok,paged", [(1, True), (7, False), (16, True), (31, False), (32, True), (33, False),
+                                         (100, True), (128, False), (129, True), (256, True), (300, False)])
 def test_append_at_model_width(mla, n_tok, paged):
-    """d_model = 7168 (the DeepSeek-V3 hidden size): up to 32 tokens take the
-    tensor-core kernel (cluster split of d_model), more take the CUDA-core
-    GEMM.  Written rows against the fp64 oracle, every other row untouched."""
+    """d_model = 7168 (the DeepSeek-V3 hidden size), the tensor-core kernel
+    (cluster split of d_model): one tile for up to 32 tokens, tiles of 128
+    tokens beyond (a partial last tile included).  Written rows against the
+    fp64 oracle, every other row untouched."""
     rng = np.random.default_rng(100 + n_tok)
     lens = rng.integers(1, 700, size=n_tok)
     wl = mi.make_random(200 + n_tok, 4, 512, 64, lens, paged=paged, poison=False, d_model=7168)
