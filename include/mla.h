@@ -219,6 +219,21 @@ int mla_decode_attn_noalloc(const mla_dims* dims, int32_t batch, const void* q, 
 int mla_out_proj(const mla_dims* dims, int32_t batch, const void* z, const void* w_uv,
                  void* o_out, void* stream);
 
+/*
+ * Self-test of the device-side bounded wait every kernel uses on its
+ * mbarriers.  Launches one CTA of 64 threads on `stream`: thread 0 waits on a
+ * barrier that nothing arrives on, giving up after `budget_cycles` SM cycles
+ * (1 .. 4e9); it then raises the CTA's abort flag and stores
+ * MLA_ERR_DEVICE_TIMEOUT in *dev_status (may be NULL), and thread 32, which
+ * waits with the full ~2 s budget on another such barrier, leaves on the
+ * flag.  dev_out (device, 2 int32) receives 1 per wait that succeeded, 0 per
+ * wait that gave up.  With `arrive` non-zero both barriers are completed
+ * first (control case: dev_out = {1, 1}, nothing reported).  Nothing faults or
+ * hangs: the kernel returns within about budget_cycles.
+ */
+int mla_selftest_bounded_wait(int64_t budget_cycles, int32_t arrive, int32_t* dev_status, int32_t* dev_out,
+                              void* stream);
+
 /* Synchronise `stream`, copy *dev_status to *host_status and return MLA_OK
  * (or MLA_ERR_CUDA if the copy failed). */
 int mla_read_status(const int32_t* dev_status, int32_t* host_status, void* stream);

@@ -11,5 +11,5 @@ from ._binding import (  # noqa: F401
     MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_BOUNDS, MLA_DECODE_FORCE_GENERIC, MLA_NOALLOC_SCRATCH_BYTES,
     mla_absorb_q, mla_append_cache, mla_decode_workspace_size, mla_decode_attn, mla_decode_attn_noalloc,
     mla_out_proj,
-    mla_read_status, mla_status_string, mla_version,
+    mla_read_status, mla_status_string, mla_version, mla_selftest_bounded_wait,
 )

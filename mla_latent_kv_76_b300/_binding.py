@@ -63,11 +63,12 @@ lib.mla_out_proj.argtypes = [_DP, _I32, _P, _P, _P, _P]
 lib.mla_decode_attn_noalloc.argtypes = [_DP, _I32, _P, _P, _P, _I32, _I32, _I64, _P, ctypes.c_float, _I32, _I32,
                                         _P, _I32, _P, _P, _P]
 lib.mla_read_status.argtypes = [_P, _P, _P]
+lib.mla_selftest_bounded_wait.argtypes = [_I64, _I32, _P, _P, _P]
 lib.mla_status_string.argtypes = [ctypes.c_int]
 lib.mla_status_string.restype = ctypes.c_char_p
 lib.mla_version.argtypes = []
 for _fn in ("mla_absorb_q", "mla_append_cache", "mla_decode_attn", "mla_out_proj", "mla_read_status",
-            "mla_version", "mla_decode_attn_noalloc"):
+            "mla_version", "mla_decode_attn_noalloc", "mla_selftest_bounded_wait"):
     getattr(lib, _fn).restype = ctypes.c_int
 
 
@@ -259,3 +260,13 @@ def mla_read_status(dev_status, stream=None) -> int:
                                _stream(stream))
     _check("mla_read_status", code)
     return int(host.value)
+
+
+def mla_selftest_bounded_wait(budget_cycles: int, arrive: bool, dev_status, dev_out, stream=None):
+    """Run the device bounded-wait self-test (include/mla.h); returns nothing,
+    results land in dev_status / dev_out on the device."""
+    _need(dev_out, 2, "dev_out")
+    code = lib.mla_selftest_bounded_wait(int(budget_cycles), 1 if arrive else 0,
+                                         _ptr(dev_status, "dev_status", (torch.int32,)),
+                                         _ptr(dev_out, "dev_out", (torch.int32,)), _stream(stream))
+    _check("mla_selftest_bounded_wait", code)

@@ -145,8 +145,10 @@ int decode_workers(const mla_dims& d, int batch, int num_workers, int flags, int
   a.d_latent = d.d_latent;
   a.d_rope = d.d_rope;
   a.batch = batch;
-  const bool use_tc = !(flags & MLA_DECODE_FORCE_GENERIC) && tc_supported(a);
-  return use_tc ? (sms / 2 > 0 ? sms / 2 : 1) : auto_workers(d, sms);
+  const bool native = !(flags & MLA_DECODE_FORCE_GENERIC);
+  if (native && tc_supported(a)) return sms / 2 > 0 ? sms / 2 : 1;  // one per SM pair
+  if (native && lh_supported(a)) return sms;                         // one per SM
+  return auto_workers(d, sms);
 }
 
 size_t decode_workspace_bytes(const mla_dims* dims, int batch, int num_workers, int flags) {
@@ -232,6 +234,7 @@ int mla_decode_attn(const mla_dims* dims, int32_t batch, const void* q, const vo
   a.status = dev_status;
   cudaStream_t s = as_stream(stream);
   if (use_tc) return from_cuda(mla::launch_decode_tc(a, s));  // partial pass + its combine
+  if (!(flags & MLA_DECODE_FORCE_GENERIC) && mla::lh_supported(a)) return from_cuda(mla::launch_decode_lh(a, s));
   cudaError_t e = mla::launch_decode_generic(a, sms, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   return from_cuda(mla::launch_combine(a, s));

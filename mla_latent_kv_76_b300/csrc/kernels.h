@@ -72,6 +72,10 @@ int generic_head_groups(int n_heads);
 // Tensor-core (tcgen05) decode for n_h = 128, d_c = 512, d_R = 64, partial pass
 // and its combine: `workers` is the number of CTA pairs (clusters of two).
 bool tc_supported(const DecodeLaunch& a);
+// Tensor-core decode for 16 heads (d_c = 512, d_R = 64): one CTA per SM, the
+// shape-generic partial layout and combine.
+cudaError_t launch_decode_lh(const DecodeLaunch& a, cudaStream_t s);
+bool lh_supported(const DecodeLaunch& a);
 
 // Split-KV workers a decode call uses (num_workers, else the automatic count
 // for its path on a device with `sms` SMs), and the workspace bytes it needs

@@ -52,6 +52,7 @@ constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
 struct Abort {
   volatile int* flag;     // shared memory, per CTA
   int32_t* status;        // global status word (may be null)
+  long long budget = kWaitCycles;  // SM cycles before `wait` gives up
 };
 
 template <bool kCluster>
@@ -62,7 +63,7 @@ MLA_DEVI bool wait(uint64_t* b, uint32_t parity, const Abort& ab) {
     if (kCluster ? mbar_test_cluster(b, parity) : mbar_test(b, parity)) return true;
     if ((it & 255u) == 0) {
       if (*ab.flag) return false;
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > ab.budget) {
         *ab.flag = 1;
         report(ab.status, MLA_ERR_DEVICE_TIMEOUT);
         return false;

@@ -117,6 +117,7 @@ CASES = [
     dict(n_heads=8, d_latent=256, d_rope=32, seqlens=[640, 1, 2000], paged=False),
     dict(n_heads=128, d_latent=512, d_rope=64, seqlens=[1, 65, 700, 2048], paged=True),
     dict(n_heads=128, d_latent=512, d_rope=64, seqlens=[4096, 4096], paged=False),
+    dict(n_heads=16, d_latent=512, d_rope=64, seqlens=[3000, 5, 0, 129, 64, 4097], paged=False),
 ]
 
 
@@ -507,3 +508,40 @@ def test_generic_decode_at_the_batch_limit(mla):
     assert st == 0
     empty = np.flatnonzero(wl.seqlens == 0)[:8]
     _check_sampled(wl, z, lse, sorted(set(list(range(0, 4096, 97)) + [4095] + list(empty))))
+
+
+# ---------------------------------------------------------------- 16-head tensor-core path
+def test_lowhead_tc_and_generic_paths_agree_with_the_oracle(mla):
+    """16 heads at d_c = 512, d_R = 64 take the one-CTA-per-SM tensor-core
+    kernel; the shape-generic kernel (forced) must give the same answers."""
+    wl = mi.make_random(2201, 16, 512, 64, [1, 700, 2048, 65, 0, 4096, 63], paged=True)
+    zt, lt, s1 = run_decode(mla, wl)
+    zg, lg, s2 = run_decode(mla, wl, flags=1)   # MLA_DECODE_FORCE_GENERIC
+    assert s1 == 0 and s2 == 0
+    check_decode(wl, zt, lt)
+    check_decode(wl, zg, lg)
+
+
+def test_lowhead_tc_growing_scores_trigger_rescaling(mla):
+    """Rows growing along the sequence move the running maximum block after
+    block on the 16-head kernel too (its O^T columns are rescaled per head)."""
+    wl = mi.make_random(2202, 16, 512, 64, [3000, 1500, 64], paged=False)
+    pool = orc.bf16_to_f64(wl.pool)
+    grow = (1.0 + np.arange(pool.shape[1]) / 256.0)[None, :, None]
+    wl.pool = orc.round_bf16_bits(np.where(np.isnan(pool), 0.0, pool) * grow)
+    for workers in (0, 1, 5):
+        z, lse, st = run_decode(mla, wl, num_workers=workers)
+        assert st == 0
+        check_decode(wl, z, lse)
+
+
+def test_lowhead_tc_zero_query_gives_the_mean_of_visible_rows(mla):
+    wl = mi.make_random(2203, 16, 512, 64, [1, 63, 64, 65, 300], paged=True)
+    wl.q = np.zeros_like(wl.q)
+    z, lse, st = run_decode(mla, wl, num_workers=3)
+    assert st == 0
+    for b, L in enumerate(wl.seqlens):
+        rows = orc.gather_rows(wl.pool, b, int(L), wl.block_table, 64, 0)
+        want = rows[:, :wl.d_latent].mean(0)
+        assert np.allclose(z[b], want[None, :], rtol=0, atol=1e-5 * max(1.0, np.abs(want).max()))
+        assert np.allclose(lse[b], math.log(L), atol=1e-5)
