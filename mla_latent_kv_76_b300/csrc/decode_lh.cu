@@ -61,7 +61,7 @@ constexpr uint32_t kColS = 0, kColO = 128, kColQ = 192;
 // barriers
 constexpr int kBarFull = 0, kBarEmpty = 3, kBarFix = 6, kBarSfull = 9, kBarSfree = 11, kBarPfull = 13,
               kBarPfree = 15, kBarQready = 17, kBarQzero = 18, kBarOcomp = 19, kBarEvt = 20, kBarEvtDone = 21,
-              kBarDrained = 22;
+              kBarDrained = 22, kBarDrainedV = 23;
 constexpr int kNumBars = 24;
 
 enum { kEvtRescale = 1, kEvtEpilogue = 2, kEvtExit = 3 };
@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bars[kBarEvt], 1);
     tc::mbar_init(&bars[kBarEvtDone], 128);
     tc::mbar_init(&bars[kBarDrained], 1);
+    tc::mbar_init(&bars[kBarDrainedV], 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -243,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars[kBarEmpty + st]);
       }
     }
-  } else if (warp >= 5 && warp <= 7) {
-    // -------------------------------------------------------------- zero query rows 32-127 of TMEM once
+  } else if (warp == 6 || warp == 7) {
+    // -------------------------------------------------------------- zero query rows 64-127 of TMEM once
     const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t z[32];
 #pragma unroll
@@ -255,13 +256,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_before();
     tc::mbar_arrive(&bars[kBarQzero]);
   }
-  else if (warp == 1) {
+  else if (warp == 1 || warp == 5) {
+    if (warp == 5) {  // zero query rows 32-63 of TMEM once, then lane 0 issues the value MMAs
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll 1
+      for (int c = 0; c < 9; ++c) tc::tmem_st32(tb + (32u << 16) + kColQ + 32 * c, z);
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars[kBarQzero]);
+    }
     if (lane == 0) {
-      // ------------------------------------------------------------ MMA issue
+      // ------------------------------------------------------------ MMA issue: warp 1 the scores,
+      // warp 5 the values (two issuing threads, so a value product waiting for
+      // its softmax never sits behind the next block's score in one thread's
+      // blocking issue; each thread's commits track its own MMAs)
       constexpr uint32_t idS = tc::idesc_bf16(128, kBlk, 0, 0);  // Q (TMEM) x block rows (K-major)
       constexpr uint32_t idV = tc::idesc_bf16(128, kH, 1, 0);    // C^T (MN-major) x P^T (K-major)
       int ev = 0, oc = 0, ntail[kMaxSlots] = {0, 0, 0};
-      bool ok = tc::wait<false>(&bars[kBarQzero], 0, ab);
+      bool ok = warp == 5 || tc::wait<false>(&bars[kBarQzero], 0, ab);
       auto post = [&](int type, int a0, int a1) -> bool {  // one event at a time
         evt_desc[0] = type;
         evt_desc[1] = a0;
@@ -315,24 +329,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       int m = 0, k = 0;
-      for (int64_t x = lo; x < hi && ok; ++k) {
-        const Seg s = seg_at(pre, B, x, hi, p, cap);
-        x += s.ntile;
-        if (!tc::wait<false>(&bars[kBarQready], k & 1, ab)) break;
-        // score of block j + 1 goes out before the value of block j, so the
-        // softmax of one block overlaps the score MMAs of the next
-        ok = score(m, s, s.t_begin);
-        for (int j = 0; j < s.ntile && ok; ++j) {
-          if (j + 1 < s.ntile) ok = score(m + j + 1, s, s.t_begin + j + 1);
-          ok = ok && value(m + j, j == 0);
+      if (warp == 1) {
+        for (int64_t x = lo; x < hi && ok; ++k) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          if (!tc::wait<false>(&bars[kBarQready], k & 1, ab)) break;
+          for (int j = 0; j < s.ntile && ok; ++j) ok = score(m + j, s, s.t_begin + j);
+          m += s.ntile;
         }
-        m += s.ntile;
-        // segment end: the partial goes out before the next segment overwrites O
-        if (!ok || !drain() || !post(kEvtEpilogue, k % kStatBufs, (int)(g + s.b))) break;
+        tc::mma_commit(&bars[kBarDrained]);
+        tc::wait_drain<false>(&bars[kBarDrained], 0, ab);
+      } else {
+        for (int64_t x = lo; x < hi && ok; ++k) {
+          const Seg s = seg_at(pre, B, x, hi, p, cap);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j) ok = value(m + j, j == 0);
+          m += s.ntile;
+          // segment end: the partial goes out before the next segment overwrites O
+          if (!ok || !drain() || !post(kEvtEpilogue, k % kStatBufs, (int)(g + s.b))) break;
+        }
+        post(kEvtExit, 0, 0);
+        tc::mma_commit(&bars[kBarDrainedV]);
+        tc::wait_drain<false>(&bars[kBarDrainedV], 0, ab);
       }
-      post(kEvtExit, 0, 0);
-      tc::mma_commit(&bars[kBarDrained]);
-      tc::wait_drain<false>(&bars[kBarDrained], 0, ab);
     }
   } else if (warp == 4) {
     // -------------------------------------------------------------- query loads and softmax (lane = head)
