@@ -96,6 +96,8 @@ struct LhParams {
   float* o_part;    // [(G + B)][16][512]  o / lq
   float* lse_part;  // [(G + B)][16]       natural log
   int32_t* status;
+  int32_t* plan_hdr;  // [plan kind 0 (even split), tiles T, workers G] for the combine
+  int32_t* seqplan;   // [B][2] for the combine: first and last worker whose tiles meet sequence b
 };
 
 struct Seg {
@@ -169,6 +171,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const tc::Abort ab{abort_flag, p.status};
   const int64_t T = pre[B];
   const int64_t lo = worker_begin(g, T, G), hi = worker_begin(g + 1, T, G);
+  if (g == 0) {  // the plan for the combine: the workers whose tiles meet each sequence
+    for (int b = tid; b < B; b += kThreads) {
+      const int t = pre[b + 1] - pre[b];
+      p.seqplan[2 * b] = t > 0 ? worker_of(pre[b], T, G) : 0;
+      p.seqplan[2 * b + 1] = t > 0 ? worker_of(pre[b + 1] - 1, T, G) : -1;
+    }
+    if (tid == 0) {
+      p.plan_hdr[0] = 0;
+      p.plan_hdr[1] = (int)T;
+      p.plan_hdr[2] = G;
+    }
+  }
+  // the combine may be scheduled now; it waits for this grid to finish before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t ring = smem_u32(sm);
   const uint32_t pbuf = smem_u32(sm + L.off_p);
 
@@ -382,7 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bars[kBarQready]);
+        if (lane == 0) {
+          tc::mbar_arrive(&bars[kBarQready]);
+          // the next segment's query (18 KB) is warmed in L2 a whole segment ahead
+          if (x < hi) tc::prefetch_l2(p.q + (int64_t)seq_of_tile(pre, B, x) * kH * kD, (uint32_t)(kH * kD * 2));
+        }
       }
       float m_ref = -INFINITY, l = 0.f, lq = 0.f;
       for (int j = 0; j < s.ntile; ++j, ++m) {
@@ -516,6 +536,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ combine
+// lse = log sum_s exp(lse_s);  z = sum_s exp(lse_s - lse) o_s over the partials
+// of the workers first..last that the partial pass recorded for sequence b
+// (workers without tiles in between wrote nothing).  Block = sequence, warp =
+// head, lane = 16 latent columns.
+template <bool ZF32>
+__global__ void __launch_bounds__(512) combine_lh_kernel(const DecodeLaunch a) {
+  // launched as a programmatic dependent of the partial pass: wait for it (and
+  // its memory) before reading anything it wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.plan_flag[1], G = a.plan_flag[2];
+  const int g0 = a.seqplan[2 * b], g1 = a.seqplan[2 * b + 1];
+  float* zf = static_cast<float*>(a.z_out) + ((int64_t)b * kH + h) * kDC + lane * 16;
+  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(a.z_out) + ((int64_t)b * kH + h) * kDC + lane * 16;
+  // a partial pass that gave up on a bounded wait left partials unwritten: the
+  // outputs are NaN then, not stale numbers
+  const bool failed = a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) == MLA_ERR_DEVICE_TIMEOUT;
+  if (g1 < g0 || failed) {
+    const float zv = failed ? __int_as_float(0x7fc00000) : 0.f;
+    for (int d = 0; d < 16; ++d) {
+      if (ZF32) zf[d] = zv; else zb[d] = __float2bfloat16_rn(zv);
+    }
+    if (lane == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = failed ? zv : -INFINITY;
+    return;
+  }
+  auto live = [&](int g) { return worker_begin(g + 1, T, G) > worker_begin(g, T, G); };
+  float mx = -INFINITY;
+  for (int g = g0; g <= g1; ++g)
+    if (live(g)) mx = fmaxf(mx, a.lse_part[((int64_t)g + b) * kH + h]);
+  float sum = 0.f;
+  for (int g = g0; g <= g1; ++g)
+    if (live(g)) sum += expf(a.lse_part[((int64_t)g + b) * kH + h] - mx);
+  const float lse = mx + logf(sum);
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g = g0; g <= g1; ++g) {
+    if (!live(g)) continue;
+    const int64_t slot = (int64_t)g + b;
+    const float w = expf(a.lse_part[slot * kH + h] - lse);
+    const float4* src = reinterpret_cast<const float4*>(a.o_part + (slot * kH + h) * kDC + lane * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = src[i];
+      acc[i].x += w * v.x;
+      acc[i].y += w * v.y;
+      acc[i].z += w * v.z;
+      acc[i].w += w * v.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (ZF32) {
+      reinterpret_cast<float4*>(zf)[i] = acc[i];
+    } else {
+      reinterpret_cast<uint2*>(zb)[i] = make_uint2(pack_bf16x2(acc[i].x, acc[i].y), pack_bf16x2(acc[i].z, acc[i].w));
+    }
+  }
+  if (lane == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = lse;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -571,13 +653,26 @@ cudaError_t launch_decode_lh(const DecodeLaunch& a, cudaStream_t s) {
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
   p.status = a.status;
+  p.plan_hdr = a.plan_flag;
+  p.seqplan = a.seqplan;
   const int smem = lh_layout(p.slots, a.batch).total;
   cudaError_t e = ensure_smem<decode_lh_kernel>(smem);
   if (e != cudaSuccess) return e;
   decode_lh_kernel<<<a.workers, kThreads, smem, s>>>(map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_combine(a, s);
+  // the combine as a programmatic dependent launch (see the 128-head path)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.batch);
+  cfg.blockDim = dim3(512);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.z_is_fp32 ? cudaLaunchKernelEx(&cfg, combine_lh_kernel<true>, a)
+                     : cudaLaunchKernelEx(&cfg, combine_lh_kernel<false>, a);
 }
 
 }  // namespace mla
