@@ -381,17 +381,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the segment's query into TMEM (the previous segment's scores are done:
       // this warp has read its last S)
       {
+        // nine rounds of 128 bytes per row, the loads of round c + 1 in flight
+        // while round c is stored (one round at a time took ~1 us of latency each)
         const uint4* row = reinterpret_cast<const uint4*>(p.q + ((int64_t)s.b * kH + (h & (kH - 1))) * kD);
-#pragma unroll 1
+        uint4 v[2][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[0][i] = h < kH ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
         for (int c = 0; c < 9; ++c) {
+          if (c + 1 < 9) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              v[(c + 1) & 1][i] = h < kH ? __ldg(row + (c + 1) * 8 + i) : make_uint4(0, 0, 0, 0);
+          }
           uint32_t r[32];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const uint4 v = h < kH ? __ldg(row + c * 8 + i) : make_uint4(0, 0, 0, 0);
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
+            r[4 * i] = v[c & 1][i].x;
+            r[4 * i + 1] = v[c & 1][i].y;
+            r[4 * i + 2] = v[c & 1][i].z;
+            r[4 * i + 3] = v[c & 1][i].w;
           }
           tc::tmem_st32(lane_t + kColQ + 32 * c, r);
         }
