@@ -60,9 +60,10 @@ constexpr uint32_t kColS = 0, kColO = 128, kColQ = 192;
 
 // barriers
 constexpr int kBarFull = 0, kBarEmpty = 3, kBarFix = 6, kBarSfull = 9, kBarSfree = 11, kBarPfull = 13,
-              kBarPfree = 15, kBarQready = 17, kBarQzero = 18, kBarOcomp = 19, kBarEvt = 20, kBarEvtDone = 21,
+              kBarPfree = 15, kBarQready = 17, kBarQzero = 24, kBarOcomp = 19, kBarEvt = 20, kBarEvtDone = 21,
               kBarDrained = 22, kBarDrainedV = 23;
-constexpr int kNumBars = 24;
+constexpr int kBarHand = 25;  // [2]: segment hand-over between the two softmax warps
+constexpr int kNumBars = 27;
 
 enum { kEvtRescale = 1, kEvtEpilogue = 2, kEvtExit = 3 };
 
@@ -152,8 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[kBarPfull + i], 1);
       tc::mbar_init(&bars[kBarPfree + i], 1);
     }
-    tc::mbar_init(&bars[kBarQready], 1);
-    tc::mbar_init(&bars[kBarQzero], 96);
+    tc::mbar_init(&bars[kBarQready], 1);      // even segments' queries
+    tc::mbar_init(&bars[kBarQready + 1], 1);  // odd segments' queries
+    tc::mbar_init(&bars[kBarQzero], 64);
+    tc::mbar_init(&bars[kBarHand], 1);
+    tc::mbar_init(&bars[kBarHand + 1], 1);
     tc::mbar_init(&bars[kBarOcomp], 1);
     tc::mbar_init(&bars[kBarEvt], 1);
     tc::mbar_init(&bars[kBarEvtDone], 128);
@@ -260,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&bars[kBarEmpty + st]);
       }
     }
-  } else if (warp == 6 || warp == 7) {
-    // -------------------------------------------------------------- zero query rows 64-127 of TMEM once
+  } else if (warp == 7) {
+    // -------------------------------------------------------------- zero query rows 96-127 of TMEM once
     const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t z[32];
 #pragma unroll
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t x = lo; x < hi && ok; ++k) {
           const Seg s = seg_at(pre, B, x, hi, p, cap);
           x += s.ntile;
-          if (!tc::wait<false>(&bars[kBarQready], k & 1, ab)) break;
+          if (!tc::wait<false>(&bars[kBarQready + (k & 1)], (k >> 1) & 1, ab)) break;
           for (int j = 0; j < s.ntile && ok; ++j) ok = score(m + j, s, s.t_begin + j);
           m += s.ntile;
         }
@@ -369,50 +373,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::wait_drain<false>(&bars[kBarDrainedV], 0, ab);
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == 4 || warp == 6) {
     // -------------------------------------------------------------- query loads and softmax (lane = head)
-    const uint32_t lane_t = tb;  // TMEM lanes 0-31: head rows 0-15, zero rows 16-31
+    // Even segments on warp 4 with their query in TMEM rows 0-15, odd ones on
+    // warp 6 with rows 64-79 (rows 16-31 / 80-95 zero): the product's rows are
+    // independent, so each warp loads its next query (segment k + 2) while the
+    // other segment's scores run, and a segment change waits for no load.
+    const int par = warp == 4 ? 0 : 1;
+    const uint32_t lane_t = tb + ((uint32_t)((warp & 3) * 32) << 16);
     const int h = lane;
-    int m = 0, k = 0;
+    auto load_q = [&](int b, int kq) {
+      // nine rounds of 128 bytes per row, the loads of round c + 1 in flight
+      // while round c is stored (one round at a time took ~1 us of latency each)
+      const uint4* row = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * kH + (h & (kH - 1))) * kD);
+      uint4 v[2][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[0][i] = h < kH ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < 9; ++c) {
+        if (c + 1 < 9) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            v[(c + 1) & 1][i] = h < kH ? __ldg(row + (c + 1) * 8 + i) : make_uint4(0, 0, 0, 0);
+        }
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          r[4 * i] = v[c & 1][i].x;
+          r[4 * i + 1] = v[c & 1][i].y;
+          r[4 * i + 2] = v[c & 1][i].z;
+          r[4 * i + 3] = v[c & 1][i].w;
+        }
+        tc::tmem_st32(lane_t + kColQ + 32 * c, r);
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bars[kBarQready + (kq & 1)]);
+    };
+    {  // this warp's first segment (0 or 1)
+      int64_t x = lo;
+      if (par == 1 && x < hi) x += seg_at(pre, B, x, hi, p, cap).ntile;
+      if (x < hi) load_q(seq_of_tile(pre, B, x), par);
+    }
+    // The two warps share the S and P barriers, whose parity waits are right
+    // only for the next phase: a warp starts segment k once the other warp has
+    // read the last S of segment k - 1 (then every earlier phase has completed).
+    int m = 0, k = 0, nh = 0;
     bool ok = true;
     for (int64_t x = lo; x < hi && ok; ++k) {
       const Seg s = seg_at(pre, B, x, hi, p, cap);
       x += s.ntile;
-      // the segment's query into TMEM (the previous segment's scores are done:
-      // this warp has read its last S)
-      {
-        // nine rounds of 128 bytes per row, the loads of round c + 1 in flight
-        // while round c is stored (one round at a time took ~1 us of latency each)
-        const uint4* row = reinterpret_cast<const uint4*>(p.q + ((int64_t)s.b * kH + (h & (kH - 1))) * kD);
-        uint4 v[2][8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[0][i] = h < kH ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 9; ++c) {
-          if (c + 1 < 9) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              v[(c + 1) & 1][i] = h < kH ? __ldg(row + (c + 1) * 8 + i) : make_uint4(0, 0, 0, 0);
-          }
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            r[4 * i] = v[c & 1][i].x;
-            r[4 * i + 1] = v[c & 1][i].y;
-            r[4 * i + 2] = v[c & 1][i].z;
-            r[4 * i + 3] = v[c & 1][i].w;
-          }
-          tc::tmem_st32(lane_t + kColQ + 32 * c, r);
-        }
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(&bars[kBarQready]);
-          // the next segment's query (18 KB) is warmed in L2 a whole segment ahead
-          if (x < hi) tc::prefetch_l2(p.q + (int64_t)seq_of_tile(pre, B, x) * kH * kD, (uint32_t)(kH * kD * 2));
-        }
+      if ((k & 1) != par) {  // the other warp's segment
+        m += s.ntile;
+        continue;
       }
+      if (k >= 1 && !tc::wait<false>(&bars[kBarHand + par], (nh++) & 1, ab)) break;
+      // where segment k + 2 (this warp's next) starts; its query is warmed in L2 now
+      int64_t x2 = x;
+      if (x2 < hi) x2 += seg_at(pre, B, x2, hi, p, cap).ntile;
+      if (x2 < hi && lane == 0)
+        tc::prefetch_l2(p.q + (int64_t)seq_of_tile(pre, B, x2) * kH * kD, (uint32_t)(kH * kD * 2));
       float m_ref = -INFINITY, l = 0.f, lq = 0.f;
       for (int j = 0; j < s.ntile; ++j, ++m) {
         const int tt = s.t_begin + j;
@@ -427,7 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_wait_ld();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bars[kBarSfree + (m & 1)]);
+        if (lane == 0) {
+          tc::mbar_arrive(&bars[kBarSfree + (m & 1)]);
+          if (j + 1 == s.ntile && x < hi) tc::mbar_arrive(&bars[kBarHand + (par ^ 1)]);  // the next segment's warp may start
+        }
         const int nvalid = tile_rows(s, tt);
         if (nvalid < kBlk) {  // tokens past the sequence end take no weight
 #pragma unroll
@@ -495,6 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bars[kBarPfull + (m & 1)]);
       }
+      // every score of segment k is done (this warp read its last S): the rows
+      // can take segment k + 2's query
+      if (ok && x2 < hi) load_q(seq_of_tile(pre, B, x2), k + 2);
     }
   }
   else if (warp >= 8) {
@@ -522,15 +549,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st32(lane_t + kColO + 32, o[1]);
         tc::tmem_wait_st();
       } else {
-        // partial of slot a1: o / lq and lse per head, in the shape-generic layout
+        // partial of slot a1: o / lq and lse per head, in the shape-generic
+        // layout.  The accumulator is in registers now, so the MMA thread may
+        // start the next segment (overwriting it) while the stores go out.
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[kBarEvtDone]);
         const float* st = stats + a0 * 3 * kH;
+        // the 16 normalisers into registers first: read through the pointer
+        // between the global stores they would be reloaded after every store
+        float inv[kH];
+#pragma unroll
+        for (int hh = 0; hh < kH; ++hh) inv[hh] = 1.f / st[2 * kH + hh];
         float* dst = p.o_part + (int64_t)a1 * kH * kDC + r;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const int mb = i >> 4, hh = i & (kH - 1);
-          dst[hh * kDC + mb * 128] = __uint_as_float(o[i >> 5][i & 31]) / st[2 * kH + hh];
+          dst[hh * kDC + mb * 128] = __uint_as_float(o[i >> 5][i & 31]) * inv[hh];
         }
         if (warp == 8 && lane < kH) p.lse_part[(int64_t)a1 * kH + lane] = (st[lane] + log2f(st[kH + lane])) * kLn2;
+        continue;
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&bars[kBarEvtDone]);
