@@ -399,9 +399,9 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    head = Setup(torch, mi, mla, dev, HEADLINE)
+    head = Setup(torch, mi, mla, dev, args.config)
     g = head.graphs(head.step)
-    sampler = ClockSampler(local_rank) if rank == 0 else None
+    sampler = ClockSampler(local_rank) if (rank == 0 and not args.plain) else None
     if sampler:
         sampler.start()
     W = max(3, args.warmup)
@@ -454,11 +454,11 @@ def run_ours(args, rank, world, local_rank):
         head.decode(0, q=q_dev.view(torch.bfloat16))
         h_z.copy_(head.z, non_blocking=True)
 
-    for _ in range(3):
+    for _ in range(0 if args.plain else 3):
         e2e_step()
     barrier()
     e2e_runs = []
-    for _ in range(3):
+    for _ in range(0 if args.plain else 3):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(K):
@@ -466,7 +466,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         barrier()
         e2e_runs.append(e0.elapsed_time(e1) * 1e3 / K)
-    e2e_us = max_over_ranks(statistics.median(e2e_runs), dist, dev)
+    e2e_us = max_over_ranks(statistics.median(e2e_runs), dist, dev) if e2e_runs else None
     head_alg = head.alg
     head.free()
     del head
@@ -493,11 +493,13 @@ def run_ours(args, rank, world, local_rank):
     hbm = m["bound"] == "hbm"
     gbs = head_alg["bytes"] / (us * 1e-6) / 1e9
     tfs = head_alg["flops"] / (us * 1e-6) / 1e12
-    roof = {"bound": m["bound"], "kernel": "mla_decode_attn: decode_tc_kernel (split-KV partial) + combine_tc_kernel",
+    kernels = ("decode_lh_kernel (split-KV partial) + combine_lh_kernel" if wl.n_heads == 16
+               else "decode_tc_kernel (split-KV partial) + combine_tc_kernel")
+    roof = {"bound": m["bound"], "kernel": "mla_decode_attn: " + kernels,
             "achieved": round(gbs if hbm else tfs, 1),
             "peak": peaks["hbm_gbs"] if hbm else peaks["bf16_tflops"], "unit": "GB/s" if hbm else "TFLOP/s",
             "frac": round((gbs / peaks["hbm_gbs"]) if hbm else (tfs / peaks["bf16_tflops"]), 4),
-            "traffic": measured_traffic(), "peak_source": peaks["source"],
+            "traffic": measured_traffic() if args.config == HEADLINE else None, "peak_source": peaks["source"],
             "algorithmic_bytes_per_launch": head_alg["bytes"], "algorithmic_flops_per_launch": head_alg["flops"],
             "tensor_achieved_tflops": round(tfs, 1), "hbm_achieved_gbs": round(gbs, 1),
             "roofline_frac_measured": m["frac"], "t_roof_us_measured": m["t_roof_us"],
@@ -509,17 +511,19 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(us / 1e3, 6), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) cache and queries)",
-        "config": {"workload": NAMES[HEADLINE], "batch": 4, "seqlen": 131072, "n_heads": 128, "d_latent": 512,
-                   "d_rope": 64, "block_tokens": 64, "step": "one mla_decode_attn call (partial + combine)",
-                   "l2": "inputs larger than L2 (604 MB cache)",
+        "config": {"workload": NAMES[args.config], "batch": wl.batch, "tokens": head_alg["tokens"],
+                   "n_heads": wl.n_heads, "d_latent": wl.d_latent, "d_rope": wl.d_rope, "block_tokens": 64,
+                   "step": "one mla_decode_attn call (partial + combine)" if args.config != "lowhead"
+                   else "mla_append_cache + mla_decode_attn",
+                   "l2": "inputs larger than L2" if args.config != "v3" else "3 rotating copies of the cache",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "timing": {"statistic": "median of the K per-step device times (CUDA events between back-to-back "
                                 "graph replays on the launching stream), max over ranks",
                    "median_us": round(us_median, 3), "mean_us": round(us_mean, 3)},
-        "tokens_per_s": round(job_tokens_per_s(4, world, us), 1),
+        "tokens_per_s": round(job_tokens_per_s(wl.batch, world, us), 1),
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+        "e2e": None if e2e_us is None else {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "runs": [round(x, 1) for x in e2e_runs],
                 "path": "eager mla_decode_attn call; q and seqlens copied in from pinned host memory, z copied out"},
         "configs": records,
@@ -613,6 +617,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-others", action="store_true", help="skip the per-configuration records and the chain")
+    ap.add_argument("--config", choices=RECORD_CONFIGS, default=HEADLINE,
+                    help="workload of the timed region (default: the long-context headline)")
+    ap.add_argument("--plain", action="store_true",
+                    help="only the timed region: no clock sampling, no end-to-end runs (for profiler runs)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(1)))
