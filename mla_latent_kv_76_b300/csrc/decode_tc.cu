@@ -95,7 +95,11 @@ constexpr int kOffPrefix = kOffMisc + 64;          // lens[B], pre[B + 1], W[B +
 constexpr int kBarCfull = 0, kBarCempty = 3, kBarSfull = 20, kBarSfree = 22, kBarQready = 24, kBarPfree = 25,
               kBarScDrained = 29, kBarXmax = 30, kBarLsum = 32, kBarStgFull = 33, kBarStgFree = 35, kBarQrope = 37;
 // value CTA barriers
-constexpr int kBarFull = 0, kBarEmpty = 2, kBarFix = 4, kBarPfull = 6, kBarOcomp = 14, kBarEvt = 15,
+// kBarRingFree + t mirrors the score CTA's kBarCempty + t (same offset; the
+// score MMA thread's commits arrive on both): the value CTA's ring helper
+// waits on it before loading into the score CTA's slot t
+constexpr int kBarRingFree = kBarCempty;
+constexpr int kBarFull = 0, kBarEmpty = 10, kBarFix = 12, kBarPfull = 6, kBarOcomp = 14, kBarEvt = 15,
               kBarEvtdone = 16, kBarVcDrained = 17;
 
 // TMEM columns
@@ -242,8 +246,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
       for (int i = 0; i < kVStages; ++i) {
         tc::mbar_init(&bars[kBarFull + i], 1);  // the producer's expect_tx (+ the copy's bytes)
-        tc::mbar_init(&bars[kBarEmpty + i], 1 + 64);
-        tc::mbar_init(&bars[kBarFix + i], 64);
+        tc::mbar_init(&bars[kBarEmpty + i], 1 + 32);
+        tc::mbar_init(&bars[kBarFix + i], 32);
       }
       for (int i = 0; i < kPBufs; ++i) {
         tc::mbar_init(&bars[kBarPfull + i], 1);  // the score CTA's expect_tx arrival + the copy
@@ -252,6 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_init(&bars[kBarEvt], 1);
       tc::mbar_init(&bars[kBarEvtdone], 256);
       tc::mbar_init(&bars[kBarVcDrained], 1);
+      for (int i = 0; i < kSlots; ++i) tc::mbar_init(&bars[kBarRingFree + i], 1);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -345,11 +350,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   tc::mbar_arrive(fb);
                   continue;
                 }
+                // this CTA copies the first half's boxes; the value CTA's ring helper
+                // copies the second half's into this slot (both signal this barrier),
+                // so the two SMs' TMA units share the slot's six copies
                 tc::mbar_expect_tx(fb, nvalid * 3 * kChunkBytes);
-                for (int cc = 0; cc < 3; ++cc)
-                  for (int w = 0; w < nh; ++w)
-                    if (blk[w] >= 0)
-                      tc::tma_load_4d(dst + cc * kChunk128 + w * kChunkBytes, &map_s, 0, 0, 3 * t + cc, blk[w], fb);
+                if (blk[0] >= 0)
+                  for (int cc = 0; cc < 3; ++cc)
+                    tc::tma_load_4d(dst + cc * kChunk128, &map_s, 0, 0, 3 * t + cc, blk[0], fb);
               } else {
                 // contiguous cache: 128 tokens x chunks 3t .. 3t + 2, chunk-major (rows
                 // past the sequence are masked by the softmax; past the allocation they
@@ -396,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc::tmem_cp_128x256b(tb + kColQ + c * 32 + kk * 8,
                                          tc::smem_desc(ring + t * kSlotBytes + cc * kChunk128 + kk * 32, 16, 1024));
               }
-              tc::mma_commit(&bars[kBarCempty + t]);
+              tc::mma_commit_multicast(&bars[kBarCempty + t], 3);  // and the value CTA's mirror
             }
             if (!ok || !tc::wait<false>(&bars[kBarQrope], 0, ab)) break;
           } else if (!tc::wait<false>(&bars[kBarQready], (k - 1) & 1, ab)) {  // a later segment's query
@@ -437,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   }
                 }
               }
-              tc::mma_commit(&bars[kBarCempty + t]);
+              tc::mma_commit_multicast(&bars[kBarCempty + t], 3);  // and the value CTA's mirror
             }
             if (ok) tc::mma_commit(&bars[kBarSfull + (m & 1)]);
           }
@@ -747,9 +754,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mma_commit(&bars[kBarVcDrained]);
         tc::wait_drain<false>(&bars[kBarVcDrained], 0, ab);
       }
-    } else if (warp < 4) {
+    } else if (warp == 2) {
+      if (lane == 0 && p.paged) {
+        // ---------------------------------------------------------- ring helper (paged cache)
+        // The second 64-token half of every score slot: three 8 KB boxes into
+        // the score CTA's ring (multicast to rank 0 only), signalled on its full
+        // barrier; a slot is reloaded once the score MMAs' commit has arrived on
+        // this CTA's mirror of the slot's free barrier.
+        bool ok = true;
+        int m = 0;
+        for (int64_t x = lo; x < hi && ok;) {
+          const Seg s = seg_at(pre, lens, B, x, hi);
+          x += s.ntile;
+          for (int j = 0; j < s.ntile && ok; ++j, ++m) {
+            const int tt = s.t_begin + j;
+            const int blk = halves_of(s, tt) > 1 ? half_block(p, s, tt, 1) : -1;
+#pragma unroll 1
+            for (int t = 0; t < kSlots; ++t) {
+              if (!tc::wait<false>(&bars[kBarRingFree + t], m & 1, ab)) {  // fill m (0: the query) consumed
+                ok = false;
+                break;
+              }
+              if (blk >= 0)
+                for (int cc = 0; cc < 3; ++cc)
+                  tc::tma_load_4d_multicast(sm + kOffRing + t * kSlotBytes + cc * kChunk128 + kChunkBytes, &map_s, 0,
+                                            0, 3 * t + cc, blk, &bars[kBarCfull + t], 1);
+            }
+          }
+        }
+        // the copies land in the score CTA, which drains its ring before the
+        // final cluster barrier; this CTA leaves only after that barrier
+      }
+    } else if (warp == 3) {
       // ------------------------------------------------------------ tail zeroing
-      const int t = tid - 64;
+      const int t = tid - 96;
       int hh = 0;
       bool ok = true;
       for (int64_t x = lo; x < hi && ok;) {
@@ -768,7 +806,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               uint8_t* stg = sm + kOffStage + st * kVStageBytes;
               const int r0 = s.len & 63;
               const int per_chunk = (64 - r0) * 8;  // 16-byte pieces per chunk
-              for (int i = t; i < 8 * per_chunk; i += 64) {
+              for (int i = t; i < 8 * per_chunk; i += 32) {
                 const int c = i / per_chunk, k = i % per_chunk;
                 *reinterpret_cast<uint4*>(stg + c * kChunkBytes + (r0 + (k >> 3)) * 128 + (k & 7) * 16) =
                     make_uint4(0, 0, 0, 0);

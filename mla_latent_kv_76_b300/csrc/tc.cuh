@@ -114,6 +114,17 @@ MLA_DEVI void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
+// The same load delivered to the CTAs of `cta_mask` in the cluster: the data
+// lands at dst's offset in each destination CTA's shared memory and the
+// transaction bytes are signalled on the barrier at bar's offset there.
+MLA_DEVI void tma_load_4d_multicast(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, uint64_t* bar,
+                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
 MLA_DEVI void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
