@@ -227,7 +227,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (tid == 64) {
     if (rank == 0) {
       for (int i = 0; i < kSlots; ++i) {
-        tc::mbar_init(&bars[kBarCfull + i], 1);  // the producer's expect_tx (+ the copies' bytes)
+        // the producer's expect_tx (+ the copies' bytes), on the paged cache also
+        // the value CTA ring helper's arrival: the helper then takes part in
+        // every fill, so this CTA can never run two fills ahead of it
+        tc::mbar_init(&bars[kBarCfull + i], p.paged ? 2 : 1);
         tc::mbar_init(&bars[kBarCempty + i], 1);
       }
       tc::mbar_init(&bars[kBarQrope], 1);
@@ -763,6 +766,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this CTA's mirror of the slot's free barrier.
         bool ok = true;
         int m = 0;
+        const uint32_t r_cfull = tc::map_peer(&bars[kBarCfull], 0);
+        if (lo < hi)
+          for (int t = 0; t < kSlots; ++t) tc::mbar_arrive_cluster_addr_relaxed(r_cfull + 8 * t);  // the query's fill
         for (int64_t x = lo; x < hi && ok;) {
           const Seg s = seg_at(pre, lens, B, x, hi);
           x += s.ntile;
@@ -779,6 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 3; ++cc)
                   tc::tma_load_4d_multicast(sm + kOffRing + t * kSlotBytes + cc * kChunk128 + kChunkBytes, &map_s, 0,
                                             0, 3 * t + cc, blk, &bars[kBarCfull + t], 1);
+              tc::mbar_arrive_cluster_addr_relaxed(r_cfull + 8 * t);  // fill m + 1 has this helper's part
             }
           }
         }
