@@ -357,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // copies the second half's into this slot (both signal this barrier),
                 // so the two SMs' TMA units share the slot's six copies
                 tc::mbar_expect_tx(fb, nvalid * 3 * kChunkBytes);
-                if (blk[0] >= 0)
+                if (blk[0] >= 0 && t < kSlots - 1)  // the helper takes both halves of the last slot
                   for (int cc = 0; cc < 3; ++cc)
                     tc::tma_load_4d(dst + cc * kChunk128, &map_s, 0, 0, 3 * t + cc, blk[0], fb);
               } else {
@@ -775,6 +775,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int j = 0; j < s.ntile && ok; ++j, ++m) {
             const int tt = s.t_begin + j;
             const int blk = halves_of(s, tt) > 1 ? half_block(p, s, tt, 1) : -1;
+            const int blk0 = half_block(p, s, tt, 0);
 #pragma unroll 1
             for (int t = 0; t < kSlots; ++t) {
               if (!tc::wait<false>(&bars[kBarRingFree + t], m & 1, ab)) {  // fill m (0: the query) consumed
@@ -785,6 +786,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 3; ++cc)
                   tc::tma_load_4d_multicast(sm + kOffRing + t * kSlotBytes + cc * kChunk128 + kChunkBytes, &map_s, 0,
                                             0, 3 * t + cc, blk, &bars[kBarCfull + t], 1);
+              if (t == kSlots - 1 && blk0 >= 0)  // and the first half of the last slot
+                for (int cc = 0; cc < 3; ++cc)
+                  tc::tma_load_4d_multicast(sm + kOffRing + t * kSlotBytes + cc * kChunk128, &map_s, 0, 0, 3 * t + cc,
+                                            blk0, &bars[kBarCfull + t], 1);
               tc::mbar_arrive_cluster_addr_relaxed(r_cfull + 8 * t);  // fill m + 1 has this helper's part
             }
           }
