@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -109,6 +110,51 @@ def measured_traffic():
     except Exception:
         pass
     return None
+
+
+NCU_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+
+
+def traffic_from_ncu_raw(csv_text):
+    """Per-kernel DRAM bytes (read, write) averaged over the captured launches,
+    from `ncu -i REPORT --page raw --csv` (a header row, a units row, then one
+    row per launch)."""
+    import csv
+    import io
+    rows = list(csv.reader(io.StringIO(csv_text)))
+    rows = [r for r in rows if r and not r[0].startswith("==")]
+    head, units, data = rows[0], rows[1], rows[2:]
+    col = {name: i for i, name in enumerate(head)}
+    k_name = col["Kernel Name"]
+    out = {}
+    for r in data:
+        m = re.search(r"([A-Za-z_]\w*_kernel)", r[k_name])
+        name = m.group(1) if m else r[k_name]
+        acc = out.setdefault(name, {"read": 0.0, "write": 0.0, "launches": 0})
+        for key, metric in (("read", "dram__bytes_read.sum"), ("write", "dram__bytes_write.sum")):
+            i = col[metric]
+            acc[key] += float(r[i].replace(",", "")) * NCU_UNITS[units[i]]
+        acc["launches"] += 1
+    return {k: {"read": v["read"] / v["launches"], "write": v["write"] / v["launches"], "launches": v["launches"]}
+            for k, v in out.items()}
+
+
+def write_traffic_record(raw_csv_path, hash_path, command):
+    """profiles/decode_traffic.json from an ncu capture of the headline: the
+    source hash is the one bench.py computed on the capturing machine, in the
+    same run, from the sources the capture executed."""
+    with open(raw_csv_path) as f:
+        per = traffic_from_ncu_raw(f.read())
+    with open(hash_path) as f:
+        h = f.read().strip()
+    total = sum(v["read"] + v["write"] for v in per.values())
+    rec = {"source_hash": h, "dram_bytes_per_launch": total,
+           "detail": {k: {"read": v["read"], "write": v["write"]} for k, v in sorted(per.items())},
+           "workload": NAMES[HEADLINE] + " (the bench headline)", "command": command}
+    with open(os.path.join(ROOT, "profiles", "decode_traffic.json"), "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 class ClockSampler:
@@ -628,7 +674,18 @@ def main():
                     help="workload of the timed region (default: the long-context headline)")
     ap.add_argument("--plain", action="store_true",
                     help="only the timed region: no clock sampling, no end-to-end runs (for profiler runs)")
+    ap.add_argument("--print-source-hash", action="store_true",
+                    help="print the hash of the decode sources and exit (taken beside an ncu capture)")
+    ap.add_argument("--write-traffic", nargs=3, metavar=("RAW_CSV", "HASH_FILE", "COMMAND"),
+                    help="write profiles/decode_traffic.json from an ncu raw-page CSV export of the headline "
+                         "capture and the source hash printed in the same run")
     args = ap.parse_args()
+    if args.print_source_hash:
+        print(decode_source_hash())
+        return
+    if args.write_traffic:
+        print(json.dumps(write_traffic_record(*args.write_traffic)))
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(1)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

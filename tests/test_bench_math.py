@@ -58,3 +58,25 @@ def test_traffic_is_reported_only_for_the_sources_it_was_taken_on(tmp_path, monk
     assert bench.measured_traffic() == pytest.approx(97.86e6)
     monkeypatch.setattr(bench, "decode_source_hash", lambda: "changed")
     assert bench.measured_traffic() is None
+
+
+def test_traffic_record_is_computed_from_the_ncu_export(tmp_path, monkeypatch):
+    raw = "\n".join([
+        '"ID","Kernel Name","Block Size","dram__bytes_read.sum","dram__bytes_write.sum"',
+        '"","","","Mbyte","Kbyte"',
+        '"0","mla::(anonymous namespace)::decode_tc_kernel(CUtensorMap, CUtensorMap)","(384, 1, 1)","605.24","3,579.39"',
+        '"1","void mla::(anonymous namespace)::combine_tc_kernel<false>(mla::DecodeLaunch)","(128, 1, 1)","19.01","0"',
+    ])
+    per = bench.traffic_from_ncu_raw(raw)
+    assert per["decode_tc_kernel"]["read"] == pytest.approx(605.24e6)
+    assert per["decode_tc_kernel"]["write"] == pytest.approx(3579.39e3)
+    assert per["combine_tc_kernel"]["read"] == pytest.approx(19.01e6) and per["combine_tc_kernel"]["write"] == 0
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "raw.csv").write_text(raw)
+    (tmp_path / "hash.txt").write_text("0123456789abcdef\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = bench.write_traffic_record(str(tmp_path / "raw.csv"), str(tmp_path / "hash.txt"), "ncu ...")
+    assert rec["source_hash"] == "0123456789abcdef"
+    assert rec["dram_bytes_per_launch"] == pytest.approx(605.24e6 + 3579.39e3 + 19.01e6)
+    monkeypatch.setattr(bench, "decode_source_hash", lambda: "0123456789abcdef")
+    assert bench.measured_traffic() == pytest.approx(rec["dram_bytes_per_launch"])
