@@ -902,9 +902,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // 512 contiguous bytes per warp.  Partials are merged kRound at a time, all
 // their loads in flight together: 4 for plans with many partials per sequence;
 // 2 for batches of many short splits, where the 64-register build keeps eight
-// blocks per SM resident instead of four (fewer waves of blocks).
+// blocks per SM resident instead of four (fewer waves of blocks).  (A minimum
+// of 0 blocks leaves the four-partial build's register budget unconstrained.)
 template <bool ZF32, int kRound>
-__global__ void __launch_bounds__(128, kRound <= 2 ? 8 : 1) combine_tc_kernel(const DecodeLaunch a) {
+__global__ void __launch_bounds__(128, kRound <= 2 ? 8 : 0) combine_tc_kernel(const DecodeLaunch a) {
   const int jg = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
   // launched as a programmatic dependent of the partial pass: wait for it (and
   // its memory) before reading anything it wrote
