@@ -899,13 +899,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // L = sum_s l_s 2^(m_s - M), Lq = sum_s lq_s 2^(m_s - M),
 // z = sum_s 2^(m_s - M) O_s / Lq, lse = (M + log2 L) ln 2.
 // Block (column group of 16, sequence b), thread = head: the partial reads are
-// 512 contiguous bytes per warp.  Partials are merged kRound at a time, all
-// their loads in flight together: 4 for plans with many partials per sequence;
-// 2 for batches of many short splits, where the 64-register build keeps eight
-// blocks per SM resident instead of four (fewer waves of blocks).  (A minimum
-// of 0 blocks leaves the four-partial build's register budget unconstrained.)
-template <bool ZF32, int kRound>
-__global__ void __launch_bounds__(128, kRound <= 2 ? 8 : 0) combine_tc_kernel(const DecodeLaunch a) {
+// 512 contiguous bytes per warp.
+template <bool ZF32>
+__global__ void __launch_bounds__(128) combine_tc_kernel(const DecodeLaunch a) {
   const int jg = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
   // launched as a programmatic dependent of the partial pass: wait for it (and
   // its memory) before reading anything it wrote
@@ -931,17 +927,17 @@ __global__ void __launch_bounds__(128, kRound <= 2 ? 8 : 0) combine_tc_kernel(co
     if (jg == 0 && a.lse_out) a.lse_out[(int64_t)b * kH + h] = failed ? zv : -INFINITY;
     return;
   }
-  // partials kRound at a time, all their loads in flight together; the running
+  // partials four at a time, all their loads in flight together; the running
   // maximum M moves as chunks arrive (acc and L rescaled by 2^(M_old - M_new))
   float M = -INFINITY, L = 0.f, Lq = 0.f;
   float4 acc[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t g = g0; g <= g1; g += kRound) {
-    float mv[kRound], lv[kRound], lqv[kRound];
-    float4 v[kRound][4];
+  for (int64_t g = g0; g <= g1; g += 4) {
+    float mv[4], lv[4], lqv[4];
+    float4 v[4][4];
 #pragma unroll
-    for (int u = 0; u < kRound; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int64_t gg = g + u;
       const int64_t slot = aligned ? gg : gg + b;
       const bool ok = gg <= g1 && (aligned || worker_begin((int)gg + 1, T, G) > worker_begin((int)gg, T, G));
@@ -959,9 +955,7 @@ __global__ void __launch_bounds__(128, kRound <= 2 ? 8 : 0) combine_tc_kernel(co
         for (int i = 0; i < 4; ++i) v[u][i] = src[i * kH];
       }
     }
-    float Mn = M;
-#pragma unroll
-    for (int u = 0; u < kRound; ++u) Mn = fmaxf(Mn, mv[u]);
+    const float Mn = fmaxf(M, fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])));
     if (Mn == -INFINITY) continue;
     const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
     L *= sc;
@@ -974,7 +968,7 @@ __global__ void __launch_bounds__(128, kRound <= 2 ? 8 : 0) combine_tc_kernel(co
       acc[i].w *= sc;
     }
 #pragma unroll
-    for (int u = 0; u < kRound; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const float w = (mv[u] == -INFINITY) ? 0.f : exp2f(mv[u] - Mn);
       L += w * lv[u];
       Lq += w * lqv[u];
@@ -1095,13 +1089,8 @@ cudaError_t launch_decode_tc(const DecodeLaunch& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // many sequences over the workers: mostly two or three partials each (the even
-  // split of the tile list), merged two at a time by the lighter build
-  if (2 * a.batch >= a.workers)
-    return a.z_is_fp32 ? cudaLaunchKernelEx(&cfg, combine_tc_kernel<true, 2>, a)
-                       : cudaLaunchKernelEx(&cfg, combine_tc_kernel<false, 2>, a);
-  return a.z_is_fp32 ? cudaLaunchKernelEx(&cfg, combine_tc_kernel<true, 4>, a)
-                     : cudaLaunchKernelEx(&cfg, combine_tc_kernel<false, 4>, a);
+  return a.z_is_fp32 ? cudaLaunchKernelEx(&cfg, combine_tc_kernel<true>, a)
+                     : cudaLaunchKernelEx(&cfg, combine_tc_kernel<false>, a);
 }
 
 }  // namespace mla
