@@ -19,24 +19,27 @@
 // Every cache byte is read from HBM once by the score CTA; the value CTA
 // re-reads the latent columns a few microseconds later, from L2.
 //
-// Score CTA, 384 threads: warp 0 TMA (3 ring slots, each three 64-column
-// chunks of 128 tokens, 128-byte swizzle; lane c issues chunk c; the first
+// Score CTA, 384 threads: warp 0 lane 0 TMA producer (a ring of 3 slots,
+// each three 64-column chunks of 128 tokens, 128-byte swizzle; the first
 // segment's query arrives through the ring ahead of tile 0), warp 1 MMA issue
 // (S double-buffered in TMEM; one barrier wait and one commit per 12 MMAs),
 // warps 4-7 / 8-11 softmax for token columns 0-63 / 64-127 (thread = head),
 // warps 2 / 3 ship each warpgroup's P to the value CTA as one bulk copy.
-// Value CTA: warp 0 TMA (2 stages of 64 tokens x 512 columns; lane c issues
-// column chunk c), warp 1 MMA,
-// warps 2-3 zero the rows past the sequence end in the last half tile (NaN
+// Value CTA: warp 0 lane 0 TMA (2 stages of 64 tokens x 512 columns, one 64 KB
+// box each), warp 1 MMA, warp 2 lane 0 the ring helper (paged cache: it loads
+// part of every score slot into the score CTA's ring, multicast to rank 0),
+// warp 3 zeroes the rows past the sequence end in the last half tile (NaN
 // garbage must not meet a zero weight), warps 4-11 rescale O and write the
 // segment's partial (thread = head, two column halves).  The value MMA thread
 // frees the score CTA's staging once a P has landed, and its commit after the
 // MMAs that read a P buffer arrives on the score CTA's barrier for that buffer.
 //
-// Copies are issued from several lanes because one issuing thread keeps only
-// one or two bulk copies moving at a time (measured on B300: ~30 GB/s per
-// thread with 8 KB copies, ~85 GB/s with four issuers), far below what an SM
-// can take in.
+// Copies are few and large: an SM's TMA unit completes a roughly fixed number
+// of copies per microsecond whatever their size up to ~24 KB (measured on
+// B300), and copies issued from several lanes of one warp were slower than
+// from one thread.  On the contiguous cache a slot is one 4-D box; on the
+// paged cache a chunk's two 64-token halves come from unrelated blocks, so a
+// slot takes six 8 KB boxes, shared between the two SMs' TMA units.
 //
 // Online softmax with a lazily updated reference maximum m_ref (base 2):
 // P = 2^(x - m_ref); m_ref moves, and O and the weight sums are rescaled, only
@@ -353,9 +356,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   tc::mbar_arrive(fb);
                   continue;
                 }
-                // this CTA copies the first half's boxes; the value CTA's ring helper
-                // copies the second half's into this slot (both signal this barrier),
-                // so the two SMs' TMA units share the slot's six copies
+                // this CTA copies the first half's boxes of slots 0 and 1; the value
+                // CTA's ring helper copies the rest into this slot (both signal this
+                // barrier), so the two SMs' TMA units share the tile's copies
                 tc::mbar_expect_tx(fb, nvalid * 3 * kChunkBytes);
                 if (blk[0] >= 0 && t < kSlots - 1)  // the helper takes both halves of the last slot
                   for (int cc = 0; cc < 3; ++cc)
@@ -760,10 +763,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 2) {
       if (lane == 0 && p.paged) {
         // ---------------------------------------------------------- ring helper (paged cache)
-        // The second 64-token half of every score slot: three 8 KB boxes into
-        // the score CTA's ring (multicast to rank 0 only), signalled on its full
-        // barrier; a slot is reloaded once the score MMAs' commit has arrived on
-        // this CTA's mirror of the slot's free barrier.
+        // The second 64-token half of every score slot, and the first half of
+        // the last slot too: three 8 KB boxes per half into the score CTA's ring
+        // (multicast to rank 0 only), signalled on its full barrier, so this SM's
+        // TMA unit takes 12 of a tile's 18 copies; a slot is reloaded once the
+        // score MMAs' commit has arrived on this CTA's mirror of the slot's free
+        // barrier.
         bool ok = true;
         int m = 0;
         const uint32_t r_cfull = tc::map_peer(&bars[kBarCfull], 0);

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
-  // one box per issuing lane: a thread keeps only one or two copies moving at a time
+  // the whole slice in one round: one box per issuing lane, all in flight together
   if (tid < 8) {
     tc::mbar_expect_tx(&bars[0], kBox);
     tc::tma_load_3d(sw + tid * kBox, &map_w, 64 * tid, 0, h, &bars[0]);
